@@ -1,0 +1,252 @@
+/*
+ * attn_oracle.c -- plain float64 CPU oracle for exact softmax attention,
+ * forward and backward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark load this file's library.  It shares no code,
+ * header or constant with the CUDA path, and the CUDA path never calls it.
+ *
+ * What it computes (per head, S query rows, S key rows, head dim d):
+ * the textbook attention function softmax(scale * Q K^T, mask) V and its
+ * gradient with respect to Q, K and V for the scalar loss sum(dO * O).
+ * The DASH pages state that the deterministic backward reaches exactly this
+ * gradient and only changes the order in which the dQ partial sums are added
+ * ("DASH: Deterministic Attention Scheduling for High-throughput Reproducible
+ * LLM Training", technical summary section 1 (problem statement) and the
+ * arXiv abstract).  So the oracle is the definition written out, step by step:
+ *
+ *   1. s_rc   = scale * sum_k q_rk k_ck               (unmasked pairs only)
+ *   2. m_r    = max_c s_rc
+ *   3. LSE_r  = m_r + ln sum_c exp(s_rc - m_r)        (natural log)
+ *   4. P_rc   = exp(s_rc - LSE_r), 0 where masked
+ *   5. O_r    = sum_c P_rc v_c
+ *   6. D_r    = sum_k dO_rk O_rk
+ *   7. dV_c   = sum_r P_rc dO_r
+ *   8. dP_rc  = sum_k dO_rk v_ck
+ *   9. dS_rc  = P_rc (dP_rc - D_r)
+ *  10. dQ_r   = scale * sum_c dS_rc k_c
+ *  11. dK_c   = scale * sum_r dS_rc q_r
+ *
+ * Masks: FULL (nothing masked) or CAUSAL (key c masked for query r when
+ * c > r; query and key sequences have the same length, so the diagonal is
+ * kept and no row is empty).
+ *
+ * Organisation: steps 1-6 and 8-10 are computed per query row r (everything
+ * they need lives in row r); steps 7 and 11 are sums over query rows for one
+ * key row c, so they are computed per key row, recomputing s_rc, P_rc, dP_rc
+ * and dS_rc from their definitions with the LSE_r and D_r of step 3 and 6.
+ * Every output element is produced by exactly one thread, summing its terms in
+ * ascending index order, so the result does not depend on the thread count.
+ *
+ * Diagnostic mode (oracle_attn_bwd_given): O and LSE are taken from the
+ * caller instead of steps 1-5, to separate backward errors from forward ones.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    int S, d, causal;
+    double scale;
+    const double *q, *k, *v, *dout; /* [S][d] each, this head */
+    const double *o_in, *lse_in;    /* diagnostic mode: given O [S][d], LSE [S] */
+    double *o, *lse, *D;            /* outputs: O [S][d], LSE [S], D [S] */
+    double *dq, *dk, *dv;           /* outputs: [S][d] each */
+} head_job;
+
+typedef struct {
+    head_job *job;
+    int tid, nthreads;
+    int phase; /* 1: query rows, 2: key rows */
+} worker_arg;
+
+static int is_masked(int causal, int r, int c) { return causal && c > r; }
+
+static double dot(const double *a, const double *b, int d)
+{
+    double acc = 0.0;
+    for (int x = 0; x < d; ++x) acc += a[x] * b[x];
+    return acc;
+}
+
+/* Steps 1-6 and 8-10 for query row r.  s and dp are scratch rows of length S. */
+static void query_row(const head_job *h, int r, double *s, double *p)
+{
+    const int S = h->S, d = h->d;
+    const double *q_r = h->q + (size_t)r * d;
+    const double *do_r = h->dout + (size_t)r * d;
+    double lse, D;
+    double *o_r = h->o + (size_t)r * d;
+
+    if (h->o_in == NULL) {
+        /* 1. scores of the unmasked keys */
+        double m = -INFINITY;
+        for (int c = 0; c < S; ++c) {
+            if (is_masked(h->causal, r, c)) continue;
+            s[c] = h->scale * dot(q_r, h->k + (size_t)c * d, d);
+            /* 2. running maximum */
+            if (s[c] > m) m = s[c];
+        }
+        /* 3. log-sum-exp */
+        double sum = 0.0;
+        for (int c = 0; c < S; ++c)
+            if (!is_masked(h->causal, r, c)) sum += exp(s[c] - m);
+        lse = m + log(sum);
+        /* 4. probabilities */
+        for (int c = 0; c < S; ++c)
+            p[c] = is_masked(h->causal, r, c) ? 0.0 : exp(s[c] - lse);
+        /* 5. output row */
+        for (int x = 0; x < d; ++x) o_r[x] = 0.0;
+        for (int c = 0; c < S; ++c) {
+            if (p[c] == 0.0) continue;
+            const double *v_c = h->v + (size_t)c * d;
+            for (int x = 0; x < d; ++x) o_r[x] += p[c] * v_c[x];
+        }
+    } else {
+        /* diagnostic mode: O and LSE given; P from the given LSE */
+        lse = h->lse_in[r];
+        for (int c = 0; c < S; ++c)
+            p[c] = is_masked(h->causal, r, c)
+                       ? 0.0
+                       : exp(h->scale * dot(q_r, h->k + (size_t)c * d, d) - lse);
+        memcpy(o_r, h->o_in + (size_t)r * d, sizeof(double) * (size_t)d);
+    }
+    h->lse[r] = lse;
+
+    /* 6. D_r = dO_r . O_r */
+    D = dot(do_r, o_r, d);
+    h->D[r] = D;
+
+    /* 8-10. dP, dS and dQ for row r (s is reused to hold dS) */
+    double *dq_r = h->dq + (size_t)r * d;
+    for (int x = 0; x < d; ++x) dq_r[x] = 0.0;
+    for (int c = 0; c < S; ++c) {
+        if (is_masked(h->causal, r, c)) continue;
+        const double dp = dot(do_r, h->v + (size_t)c * d, d); /* 8 */
+        const double ds = p[c] * (dp - D);                    /* 9 */
+        const double *k_c = h->k + (size_t)c * d;
+        for (int x = 0; x < d; ++x) dq_r[x] += ds * k_c[x];   /* 10 (sum) */
+    }
+    for (int x = 0; x < d; ++x) dq_r[x] *= h->scale;          /* 10 (scale) */
+}
+
+/* Steps 7 and 11 for key row c, using LSE_r and D_r of every query row. */
+static void key_row(const head_job *h, int c)
+{
+    const int S = h->S, d = h->d;
+    const double *k_c = h->k + (size_t)c * d;
+    const double *v_c = h->v + (size_t)c * d;
+    double *dk_c = h->dk + (size_t)c * d;
+    double *dv_c = h->dv + (size_t)c * d;
+    for (int x = 0; x < d; ++x) { dk_c[x] = 0.0; dv_c[x] = 0.0; }
+    for (int r = 0; r < S; ++r) {
+        if (is_masked(h->causal, r, c)) continue;
+        const double *q_r = h->q + (size_t)r * d;
+        const double *do_r = h->dout + (size_t)r * d;
+        const double s = h->scale * dot(q_r, k_c, d);   /* 1 */
+        const double p = exp(s - h->lse[r]);            /* 4 */
+        const double dp = dot(do_r, v_c, d);            /* 8 */
+        const double ds = p * (dp - h->D[r]);           /* 9 */
+        for (int x = 0; x < d; ++x) {
+            dv_c[x] += p * do_r[x];                     /* 7 */
+            dk_c[x] += ds * q_r[x];                     /* 11 (sum) */
+        }
+    }
+    for (int x = 0; x < d; ++x) dk_c[x] *= h->scale;   /* 11 (scale) */
+}
+
+static void *worker(void *argp)
+{
+    worker_arg *a = (worker_arg *)argp;
+    head_job *h = a->job;
+    if (a->phase == 1) {
+        double *s = (double *)malloc(sizeof(double) * (size_t)h->S);
+        double *p = (double *)malloc(sizeof(double) * (size_t)h->S);
+        if (s == NULL || p == NULL) { free(s); free(p); return (void *)1; }
+        for (int r = a->tid; r < h->S; r += a->nthreads) query_row(h, r, s, p);
+        free(s);
+        free(p);
+    } else {
+        for (int c = a->tid; c < h->S; c += a->nthreads) key_row(h, c);
+    }
+    return NULL;
+}
+
+static int run_phase(head_job *h, int phase, int nthreads)
+{
+    pthread_t th[256];
+    worker_arg args[256];
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    int failed = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        args[t].job = h;
+        args[t].tid = t;
+        args[t].nthreads = nthreads;
+        args[t].phase = phase;
+        if (t > 0 && pthread_create(&th[t], NULL, worker, &args[t]) != 0) {
+            /* fall back: run this share on the calling thread */
+            if (worker(&args[t]) != NULL) failed = 1;
+            th[t] = 0;
+        }
+    }
+    if (worker(&args[0]) != NULL) failed = 1;
+    for (int t = 1; t < nthreads; ++t) {
+        void *ret = NULL;
+        if (th[t] != 0) {
+            pthread_join(th[t], &ret);
+            if (ret != NULL) failed = 1;
+        }
+    }
+    return failed ? -1 : 0;
+}
+
+static int run_heads(int BH, int S, int d, double scale, int causal,
+                     const double *q, const double *k, const double *v,
+                     const double *dout, const double *o_in, const double *lse_in,
+                     double *o, double *lse, double *D,
+                     double *dq, double *dk, double *dv, int nthreads)
+{
+    if (BH < 0 || S < 0 || d <= 0) return -2;
+    for (int b = 0; b < BH; ++b) {
+        const size_t off = (size_t)b * (size_t)S * (size_t)d;
+        head_job h;
+        h.S = S; h.d = d; h.causal = causal; h.scale = scale;
+        h.q = q + off; h.k = k + off; h.v = v + off; h.dout = dout + off;
+        h.o_in = o_in ? o_in + off : NULL;
+        h.lse_in = lse_in ? lse_in + (size_t)b * S : NULL;
+        h.o = o + off; h.lse = lse + (size_t)b * S; h.D = D + (size_t)b * S;
+        h.dq = dq + off; h.dk = dk + off; h.dv = dv + off;
+        if (run_phase(&h, 1, nthreads) != 0) return -1;
+        if (run_phase(&h, 2, nthreads) != 0) return -1;
+    }
+    return 0;
+}
+
+/* Full forward + backward for BH independent heads, inputs [BH][S][d]. */
+int oracle_attn_fwd_bwd(int BH, int S, int d, double scale, int causal,
+                        const double *q, const double *k, const double *v,
+                        const double *dout,
+                        double *o, double *lse, double *D,
+                        double *dq, double *dk, double *dv, int nthreads)
+{
+    return run_heads(BH, S, d, scale, causal, q, k, v, dout, NULL, NULL,
+                     o, lse, D, dq, dk, dv, nthreads);
+}
+
+/* Diagnostic backward with O [BH][S][d] and LSE [BH][S] supplied by the
+ * caller (for instance the values a GPU forward produced).  o_out receives a
+ * copy of o_in, lse_out a copy of lse_in. */
+int oracle_attn_bwd_given(int BH, int S, int d, double scale, int causal,
+                          const double *q, const double *k, const double *v,
+                          const double *o_in, const double *lse_in,
+                          const double *dout,
+                          double *o_out, double *lse_out, double *D,
+                          double *dq, double *dk, double *dv, int nthreads)
+{
+    if (o_in == NULL || lse_in == NULL) return -2;
+    return run_heads(BH, S, d, scale, causal, q, k, v, dout, o_in, lse_in,
+                     o_out, lse_out, D, dq, dk, dv, nthreads);
+}
