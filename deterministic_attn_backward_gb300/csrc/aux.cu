@@ -1,0 +1,121 @@
+// aux.cu -- the two bandwidth-bound kernels around the main backward kernel.
+//
+// preprocess: D_r = sum_k dO_rk O_rk in f32 (the row term of
+//             dS = P o (dP - D)), LSE_r * log2(e) for the base-2 softmax
+//             recomputation, and the reset of everything the main kernel
+//             needs at zero (status word, dispatch counter, dQ semaphores;
+//             the f32 dQ accumulator too for the unordered atomic schedule).
+// convert:    dQ = bf16(scale * dQacc).
+// Both are grid-stride loops over 16-byte vectors, sized to a multiple of the
+// SM count by the host.
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace dab {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Sum of the bf16 products of two 16-byte vectors (8 elements each), in f32.
+// bf16 x bf16 products are exact in f32; they are added in element order.
+__device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), acc);
+    acc = fmaf(__uint_as_float(aw[i] & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u), acc);
+  }
+  return acc;
+}
+
+// One row of HD bf16 is HD/8 vectors; a warp covers 32 / (HD/8) rows at once.
+template <int HD>
+__global__ void __launch_bounds__(256) preprocess_kernel(
+    const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+    const float* __restrict__ lse, float* __restrict__ D, float* __restrict__ lse2,
+    uint32_t* __restrict__ sem, int n_sem, WsHeader* __restrict__ hdr,
+    float4* __restrict__ dqacc, long long dq_vec4, int rows) {
+  constexpr int kLanesPerRow = HD / 8;
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  const int lane = threadIdx.x & 31;
+  const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+
+  if (gtid == 0) {
+    hdr->status = 0u;
+    hdr->detail = 0u;
+    hdr->ticket = 0u;
+  }
+  for (long long i = gtid; i < n_sem; i += nthreads) sem[i] = 0u;
+  if (dqacc != nullptr) {
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long i = gtid; i < dq_vec4; i += nthreads) dqacc[i] = z;
+  }
+
+  const int sub = lane / kLanesPerRow;   // row within the warp's group
+  const int part = lane % kLanesPerRow;  // 16-byte piece of the row
+  for (long long r0 = gwarp * kRowsPerWarp; r0 < rows; r0 += nwarps * kRowsPerWarp) {
+    const long long row = r0 + sub;
+    float acc = 0.f;
+    if (row < rows) {
+      const uint4 a = reinterpret_cast<const uint4*>(o + row * HD)[part];
+      const uint4 b = reinterpret_cast<const uint4*>(dout + row * HD)[part];
+      acc = dot8_bf16(a, b);
+    }
+#pragma unroll
+    for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
+      acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && part == 0) {
+      D[row] = acc;
+      lse2[row] = lse[row] * kLog2e;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__ acc,
+                                                      uint2* __restrict__ out, long long n_vec4,
+                                                      float scale) {
+  const long long n = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec4; i += n) {
+    const float4 v = acc[i];
+    uint2 w;
+    w.x = pack_bf16x2(scale * v.x, scale * v.y);
+    w.y = pack_bf16x2(scale * v.z, scale * v.w);
+    out[i] = w;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const float* lse, float* D,
+                              float* lse2, uint32_t* sem, int n_sem, WsHeader* hdr, float* dqacc,
+                              long long dq_elems, int rows, int grid, cudaStream_t stream) {
+  float4* z = reinterpret_cast<float4*>(dqacc);
+  const long long nv = dqacc ? dq_elems / 4 : 0;
+  if (HD == 128) {
+    preprocess_kernel<128><<<grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, D, lse2,
+        sem, n_sem, hdr, z, nv, rows);
+  } else {
+    preprocess_kernel<64><<<grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, D, lse2,
+        sem, n_sem, hdr, z, nv, rows);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert(const float* dqacc, void* dq, long long elems, float scale, int grid,
+                           cudaStream_t stream) {
+  convert_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dqacc),
+                                           reinterpret_cast<uint2*>(dq), elems / 4, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace dab

@@ -1,0 +1,550 @@
+// bwd.cu -- persistent attention backward kernel for GB300 (sm_103a).
+//
+// One CTA per SM.  A CTA takes work units (one KV tile's chain, or a pair of
+// chains for the causal symmetric shift) and, for every step (KV tile i,
+// Q tile j) of a chain, computes on the tensor cores (tcgen05, operands in
+// shared memory or tensor memory, f32 accumulators in tensor memory):
+//     S^T  = K_i Q_j^T                      (128 x 128, contraction over d)
+//     P^T  = exp(scale S^T - LSE_j)         (softmax warps; causal mask)
+//     dP^T = V_i dO_j^T
+//     dV_i += P^T dO_j                      (P^T read from tensor memory)
+//     dS^T = P^T o (dP^T - D_j)             (softmax warps -> shared memory)
+//     dK_i += dS^T Q_j
+//     dQ_j partial = dS K_i                 (as dQ^T = K_i^T dS^T for d = 128)
+// dK_i and dV_i stay in tensor memory for the whole chain (the KV-chain
+// constraint of the DASH DAG model, technical summary section 2.1) and are
+// written once at its end.  The dQ partial is added to an f32 accumulator in
+// global memory by the reducer warps: for the deterministic schedules in the
+// fixed order rank(i, j) (technical summary section 1: a fixed accumulation
+// order for dQ), waiting on a per-(head, Q tile) semaphore with acquire loads
+// and publishing with a release store; for ATOMIC with unordered float adds.
+//
+// Warp roles (16 warps):
+//   warp 0      TMA producer (K_i, V_i per chain; Q_j, dO_j, LSE_j, D_j per
+//               step, double-buffered) and tensor-memory allocation
+//   warp 1      MMA issuer (one thread)
+//   warps 4-7   softmax / dS warpgroup (thread = KV row), chain epilogue
+//   warps 8-15  dQ reducers (two warpgroups, one half of the tile each)
+// Every wait is bounded: on expiry the kernel records DAB_ERR_TIMEOUT in the
+// workspace and every role drains and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tile_sched.h"
+
+namespace dab {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int kReducerWarp0 = 8;
+constexpr int kNumReducerThreads = 256;
+constexpr uint32_t kReducerBar = 1;  // named barrier id
+
+template <int HD>
+struct Cfg {
+  static constexpr int kTileBytes = kTile * HD * 2;        // one 128 x HD bf16 tile
+  static constexpr int kBlockBytes = kTile * 128;          // one [128 rows][64] block
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffQ = 2 * kTileBytes;             // 2 stages
+  static constexpr int kOffDO = 4 * kTileBytes;            // 2 stages
+  static constexpr int kOffDS = 6 * kTileBytes;            // [2][128][64] bf16
+  static constexpr int kOffLse = kOffDS + 32768;           // [2][128] f32
+  static constexpr int kOffDD = kOffLse + 1024;            // [2][128] f32
+  static constexpr int kOffBar = kOffDD + 1024;
+  static constexpr int kOffMisc = kOffBar + 256;
+  static constexpr int kSmemBytes = kOffMisc + 64;
+  // Tensor memory columns (512 allocated).
+  static constexpr uint32_t kColDV = 0;
+  static constexpr uint32_t kColDK = HD;
+  static constexpr uint32_t kColS = 2 * HD;                // S^T, then P^T (bf16, 64 cols)
+  static constexpr uint32_t kColDP = 2 * HD + 128;
+  static constexpr uint32_t kColDQ = (HD == 128) ? kColDP : 384;  // d=128 reuses dP
+  // Instruction descriptors.
+  static constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
+  static constexpr uint32_t kIdAcc = idesc_bf16(128, HD, 0, 1);  // dV, dK
+  static constexpr uint32_t kIdDQ = (HD == 128) ? idesc_bf16(128, 128, 1, 1)   // dQ^T
+                                                : idesc_bf16(128, 64, 1, 1);   // dQ
+};
+
+struct Bars {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full;
+  uint64_t dv_done, ds_free, dq_full, dq_empty;
+  uint64_t acc_full, acc_empty;
+  uint64_t unit_full[2], unit_empty[2];
+  uint64_t drain;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+struct Misc {
+  uint32_t tmem_base;
+  int abort;
+  int ring[2];
+  // Reducer-group control slots, written by the reducer leader and read by
+  // the whole group after a named barrier (so the group always takes the same
+  // path through its barriers).
+  int red_unit;
+  int red_dq_ok[2];
+  int red_sem_ok[2];
+};
+static_assert(sizeof(Misc) <= 64, "misc block");
+
+static __device__ __noinline__ bool sem_wait(const uint32_t* sem, uint32_t target, const WaitCtl& w,
+                                      uint32_t detail) {
+  uint64_t t0 = 0;
+  uint32_t it = 0;
+  while (true) {
+    if (ld_acquire_gpu(sem) == target) return true;
+    if (it == 0) t0 = globaltimer_ns();
+    if ((++it & 15u) == 0u) {
+      if (*w.abort) return false;
+      if (ld_volatile(&w.hdr->status) != 0u) {
+        *w.abort = 1;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        raise_error(w.hdr, kStatusTimeout, kDetailSem | (detail & 0xFFFFFFu));
+        *w.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
+  using C = Cfg<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
+  Misc* misc = reinterpret_cast<Misc*>(smem + C::kOffMisc);
+  float* s_lse = reinterpret_cast<float*>(smem + C::kOffLse);
+  float* s_dd = reinterpret_cast<float*>(smem + C::kOffDD);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Operand tiles need 1024-byte-aligned swizzle atoms.
+  if ((sbase & 1023u) != 0u) {
+    if (threadIdx.x == 0) raise_error(p.hdr, kStatusBounds, kDetailAlign);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1 + 4);
+      mbar_init(&bars->unit_full[s], 1);
+      mbar_init(&bars->unit_empty[s], 1 + 4 + 8);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->ds_full, 4);
+    mbar_init(&bars->dv_done, 1);
+    mbar_init(&bars->ds_free, 1);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_empty, 8);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, 4);
+    mbar_init(&bars->drain, 1);
+    misc->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&misc->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = misc->tmem_base;
+  const WaitCtl wc{&misc->abort, p.hdr, p.timeout_ns};
+  const bool deterministic = p.sched != kSchedAtomic;
+  const bool is_static = static_dispatch(p.sched);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&p.tm_q);
+      prefetch_tensormap(&p.tm_k);
+      prefetch_tensormap(&p.tm_v);
+      prefetch_tensormap(&p.tm_do);
+      int s = 0, chain = 0, uidx = 0, prevU = -1;
+      int issued[2] = {0, 0};
+      bool ok = true;
+      while (ok) {
+        int U;
+        if (is_static) {
+          U = (uidx == 0) ? (int)blockIdx.x : prevU + (int)gridDim.x;
+        } else {
+          U = (int)atomicAdd(&p.hdr->ticket, 1u);
+        }
+        if (U >= p.total_units) U = -1;
+        prevU = U;
+        const int slot = uidx & 1;
+        if (uidx >= 2 && !mbar_wait(&bars->unit_empty[slot], ((uidx >> 1) - 1) & 1, wc, 1)) break;
+        misc->ring[slot] = U;
+        mbar_arrive(&bars->unit_full[slot]);
+        ++uidx;
+        if (U < 0) break;
+        const int bh = U / p.units_per_head, u = U % p.units_per_head;
+        const int steps = unit_steps(p.sched, p.mask, p.N, u);
+        for (int t = 0; t < steps; ++t) {
+          const Step st = step(p.sched, p.mask, p.N, u, t);
+          if (st.chain_first) {
+            if (chain > 0 && !mbar_wait(&bars->kv_empty, (chain - 1) & 1, wc, 2)) { ok = false; break; }
+            mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
+            const int row = bh * p.S + st.kv * kTile;
+#pragma unroll
+            for (int db = 0; db < HD / 64; ++db) {
+              tma_load_2d(smem + C::kOffK + db * C::kBlockBytes, &p.tm_k, &bars->kv_full, db * 64, row);
+              tma_load_2d(smem + C::kOffV + db * C::kBlockBytes, &p.tm_v, &bars->kv_full, db * 64, row);
+            }
+            ++chain;
+          }
+          const int stage = s & 1;
+          if (s >= 2 && !mbar_wait(&bars->q_empty[stage], ((s >> 1) - 1) & 1, wc, 3)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->q_full[stage], 2 * C::kTileBytes + 1024);
+          const int row = bh * p.S + st.q * kTile;
+          uint8_t* sq = smem + C::kOffQ + stage * C::kTileBytes;
+          uint8_t* sdo = smem + C::kOffDO + stage * C::kTileBytes;
+#pragma unroll
+          for (int db = 0; db < HD / 64; ++db) {
+            tma_load_2d(sq + db * C::kBlockBytes, &p.tm_q, &bars->q_full[stage], db * 64, row);
+            tma_load_2d(sdo + db * C::kBlockBytes, &p.tm_do, &bars->q_full[stage], db * 64, row);
+          }
+          bulk_load(s_lse + stage * 128, p.lse2 + row, 512, &bars->q_full[stage]);
+          bulk_load(s_dd + stage * 128, p.D + row, 512, &bars->q_full[stage]);
+          ++issued[stage];
+          ++s;
+        }
+      }
+      // Teardown: every issued copy must land before the CTA may exit.
+      if (chain > 0) drain_wait(&bars->kv_full, (chain - 1) & 1, p.hdr, p.timeout_ns, 1);
+      for (int st = 0; st < 2; ++st)
+        if (issued[st] > 0) drain_wait(&bars->q_full[st], (issued[st] - 1) & 1, p.hdr, p.timeout_ns, 2);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sDS = sbase + C::kOffDS;
+      int s = 0, chain = 0, uidx = 0;
+      bool ok = true;
+      while (ok) {
+        const int slot = uidx & 1;
+        if (!mbar_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 10)) break;
+        const int U = misc->ring[slot];
+        mbar_arrive(&bars->unit_empty[slot]);
+        ++uidx;
+        if (U < 0) break;
+        const int u = U % p.units_per_head;
+        const int steps = unit_steps(p.sched, p.mask, p.N, u);
+        for (int t = 0; t < steps; ++t) {
+          const Step st = step(p.sched, p.mask, p.N, u, t);
+          const int stage = s & 1;
+          const uint32_t sQ = sbase + C::kOffQ + stage * C::kTileBytes;
+          const uint32_t sDO = sbase + C::kOffDO + stage * C::kTileBytes;
+          if (st.chain_first && !mbar_wait(&bars->kv_full, chain & 1, wc, 11)) { ok = false; break; }
+          if (!mbar_wait(&bars->q_full[stage], (s >> 1) & 1, wc, 12)) { ok = false; break; }
+          // S^T = K Q^T (the previous P^T must have been consumed by its dV MMA)
+          if (s > 0 && !mbar_wait(&bars->dv_done, (s - 1) & 1, wc, 13)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < HD / 16; ++k)
+            mma_ss(tbase + C::kColS, desc_kmajor(sK, k, 128), desc_kmajor(sQ, k, 128), C::kIdS, k > 0);
+          mma_commit(&bars->s_full);
+          // dP^T = V dO^T (for d = 128 it lands where the previous dQ^T was)
+          if (HD == 128 && s > 0 && !mbar_wait(&bars->dq_empty, (s - 1) & 1, wc, 14)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < HD / 16; ++k)
+            mma_ss(tbase + C::kColDP, desc_kmajor(sV, k, 128), desc_kmajor(sDO, k, 128), C::kIdS, k > 0);
+          mma_commit(&bars->dp_full);
+          // dV += P^T dO, P^T from tensor memory
+          if (!mbar_wait(&bars->p_full, s & 1, wc, 15)) { ok = false; break; }
+          if (st.chain_first && chain > 0 && !mbar_wait(&bars->acc_empty, (chain - 1) & 1, wc, 16)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_ts(tbase + C::kColDV, tbase + C::kColS + 8 * k, desc_mnmajor(sDO, k, 128), C::kIdAcc,
+                   !(st.chain_first && k == 0));
+          mma_commit(&bars->dv_done);
+          // dK += dS^T Q ; dQ partial
+          if (!mbar_wait(&bars->ds_full, s & 1, wc, 17)) { ok = false; break; }
+          if (HD == 64 && s > 0 && !mbar_wait(&bars->dq_empty, (s - 1) & 1, wc, 18)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_ss(tbase + C::kColDK, desc_kmajor(sDS, k, 128), desc_mnmajor(sQ, k, 128), C::kIdAcc,
+                   !(st.chain_first && k == 0));
+          mma_commit(&bars->q_empty[stage]);
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k) {
+            // d = 128: dQ^T = K^T dS^T (A = K, MN-major; B = dS^T, MN-major)
+            // d =  64: dQ   = dS K     (A = dS, MN-major; B = K, MN-major)
+            const uint64_t a = (HD == 128) ? desc_mnmajor(sK, k, 128) : desc_mnmajor(sDS, k, 128);
+            const uint64_t b = (HD == 128) ? desc_mnmajor(sDS, k, 128) : desc_mnmajor(sK, k, 128);
+            mma_ss(tbase + C::kColDQ, a, b, C::kIdDQ, k > 0);
+          }
+          mma_commit(&bars->dq_full);
+          mma_commit(&bars->ds_free);
+          if (st.chain_last) {
+            mma_commit(&bars->acc_full);
+            mma_commit(&bars->kv_empty);
+            ++chain;
+          }
+          ++s;
+        }
+      }
+      // Teardown: wait until every issued MMA has completed.
+      mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0, p.hdr, p.timeout_ns, 3);
+    }
+    __syncwarp();
+  } else if (warp >= kSoftmaxWarp0 && warp < kReducerWarp0) {
+    // ------------------------------------------------------ softmax / dS
+    const int quad = warp & 3;                 // tensor-memory lane quadrant
+    const int r = quad * 32 + lane;            // KV row of the tile
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    uint8_t* sds = smem + C::kOffDS;
+    int s = 0, chain = 0, uidx = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = uidx & 1;
+      if (!warp_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 20)) break;
+      const int U = misc->ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->unit_empty[slot]);
+      ++uidx;
+      if (U < 0) break;
+      const int bh = U / p.units_per_head, u = U % p.units_per_head;
+      const int steps = unit_steps(p.sched, p.mask, p.N, u);
+      for (int t = 0; t < steps; ++t) {
+        const Step st = step(p.sched, p.mask, p.N, u, t);
+        const int stage = s & 1;
+        const float* lse = s_lse + stage * 128;
+        const float* dd = s_dd + stage * 128;
+        const bool diag = (p.mask == kMaskCausal) && (st.kv == st.q);
+        if (!warp_wait(&bars->q_full[stage], (s >> 1) & 1, wc, 21)) { ok = false; break; }
+        if (!warp_wait(&bars->s_full, s & 1, wc, 22)) { ok = false; break; }
+        tc_fence_after();
+        // P^T = exp2(S^T * scale*log2(e) - LSE*log2(e)), packed to bf16 in place.
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_off + C::kColS + 32 * c, v);
+          uint32_t w16[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int col = 32 * c + e;
+            float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2e, -lse[col]));
+            float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2e, -lse[col + 1]));
+            if (diag) {
+              if (r > col) p0 = 0.f;
+              if (r > col + 1) p1 = 0.f;
+            }
+            w16[e >> 1] = pack_bf16x2(p0, p1);
+            pk[16 * c + (e >> 1)] = w16[e >> 1];
+          }
+          tmem_st16(tbase + lane_off + C::kColS + 16 * c, w16);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full);
+        // dS^T = P^T o (dP^T - D) -> shared memory (bf16, 128B-swizzled)
+        if (!warp_wait(&bars->dp_full, s & 1, wc, 23)) { ok = false; break; }
+        if (s > 0 && !warp_wait(&bars->ds_free, (s - 1) & 1, wc, 24)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_off + C::kColDP + 32 * c, v);
+          uint32_t w16[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int col = 32 * c + e;
+            const uint32_t pp = pk[16 * c + (e >> 1)];
+            const float p0 = __uint_as_float(pp << 16);
+            const float p1 = __uint_as_float(pp & 0xFFFF0000u);
+            const float ds0 = p0 * (__uint_as_float(v[e]) - dd[col]);
+            const float ds1 = p1 * (__uint_as_float(v[e + 1]) - dd[col + 1]);
+            w16[e >> 1] = pack_bf16x2(ds0, ds1);
+          }
+          uint8_t* rowp = sds + (c >> 1) * 16384 + r * 128;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int cc = (c & 1) * 4 + m;
+            uint4 val = make_uint4(w16[4 * m], w16[4 * m + 1], w16[4 * m + 2], w16[4 * m + 3]);
+            *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = val;
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->ds_full);
+          mbar_arrive(&bars->q_empty[stage]);
+        }
+        if (st.chain_last) {
+          // Epilogue: dV_i = bf16(dV acc), dK_i = bf16(scale * dK acc).
+          if (!warp_wait(&bars->acc_full, chain & 1, wc, 25)) { ok = false; break; }
+          tc_fence_after();
+          const size_t row = (size_t)bh * p.S + (size_t)st.kv * kTile + r;
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + lane_off + C::kColDV + 32 * c, v);
+            uint4* dst = reinterpret_cast<uint4*>(p.dv + row * HD + 32 * c);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+              dst[m] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * m]), __uint_as_float(v[8 * m + 1])),
+                                  pack_bf16x2(__uint_as_float(v[8 * m + 2]), __uint_as_float(v[8 * m + 3])),
+                                  pack_bf16x2(__uint_as_float(v[8 * m + 4]), __uint_as_float(v[8 * m + 5])),
+                                  pack_bf16x2(__uint_as_float(v[8 * m + 6]), __uint_as_float(v[8 * m + 7])));
+            tmem_ld32(tbase + lane_off + C::kColDK + 32 * c, v);
+            uint4* dstk = reinterpret_cast<uint4*>(p.dk + row * HD + 32 * c);
+            const float sc = p.scale;
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+              dstk[m] = make_uint4(
+                  pack_bf16x2(sc * __uint_as_float(v[8 * m]), sc * __uint_as_float(v[8 * m + 1])),
+                  pack_bf16x2(sc * __uint_as_float(v[8 * m + 2]), sc * __uint_as_float(v[8 * m + 3])),
+                  pack_bf16x2(sc * __uint_as_float(v[8 * m + 4]), sc * __uint_as_float(v[8 * m + 5])),
+                  pack_bf16x2(sc * __uint_as_float(v[8 * m + 6]), sc * __uint_as_float(v[8 * m + 7])));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->acc_empty);
+          ++chain;
+        }
+        ++s;
+      }
+    }
+  } else if (warp >= kReducerWarp0) {
+    // ------------------------------------------------------ dQ reducers
+    // The leader (first reducer thread) does every wait; the group follows
+    // its decisions through shared-memory slots read after a named barrier,
+    // so all 256 threads always pass the same barriers.
+    const int quad = warp & 3;
+    const int half = (warp - kReducerWarp0) >> 2;
+    const int r = quad * 32 + lane;  // tensor-memory lane: d index (d=128) or Q row (d=64)
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const bool leader = (threadIdx.x == kReducerWarp0 * 32);
+    volatile Misc* vm = misc;
+    int s = 0, uidx = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = uidx & 1;
+      if (leader) {
+        vm->red_unit = mbar_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 30) ? vm->ring[slot] : -2;
+      }
+      named_bar_sync(kReducerBar, kNumReducerThreads);
+      const int U = vm->red_unit;
+      if (lane == 0 && U != -2) mbar_arrive(&bars->unit_empty[slot]);
+      ++uidx;
+      if (U < 0) break;
+      const int bh = U / p.units_per_head, u = U % p.units_per_head;
+      const int steps = unit_steps(p.sched, p.mask, p.N, u);
+      for (int t = 0; t < steps; ++t) {
+        const Step st = step(p.sched, p.mask, p.N, u, t);
+        if (leader) vm->red_dq_ok[s & 1] = mbar_wait(&bars->dq_full, s & 1, wc, 31) ? 1 : 0;
+        named_bar_sync(kReducerBar, kNumReducerThreads);
+        if (!vm->red_dq_ok[s & 1]) { ok = false; break; }
+        tc_fence_after();
+        constexpr int kVals = (HD == 128) ? 64 : 32;
+        float val[kVals];
+        {
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < kVals / 32; ++c) {
+            tmem_ld32(tbase + lane_off + C::kColDQ + (uint32_t)(half * kVals + 32 * c), v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) val[32 * c + e] = __uint_as_float(v[e]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->dq_empty);
+        int rank = 0;
+        uint32_t* sem = p.sem + (size_t)bh * p.N + st.q;
+        if (deterministic) {
+          rank = dab::rank(p.sched, p.mask, p.N, st.kv, st.q);
+          if (leader)
+            vm->red_sem_ok[s & 1] = sem_wait(sem, (uint32_t)rank, wc, (uint32_t)(bh * p.N + st.q)) ? 1 : 0;
+          named_bar_sync(kReducerBar, kNumReducerThreads);
+          if (!vm->red_sem_ok[s & 1]) { ok = false; break; }
+        }
+        const size_t row0 = (size_t)bh * p.S + (size_t)st.q * kTile;
+        if (HD == 128) {
+          // thread = d index; values = Q rows half*64 .. half*64+63
+          float* base = p.dqacc + (row0 + (size_t)half * 64) * HD + r;
+          if (deterministic && rank == 0) {
+#pragma unroll
+            for (int q = 0; q < 64; ++q) base[(size_t)q * HD] = val[q];
+          } else {
+#pragma unroll
+            for (int q = 0; q < 64; ++q) red_add_f32(base + (size_t)q * HD, val[q]);
+          }
+        } else {
+          // thread = Q row; values = d columns half*32 .. half*32+31
+          float* base = p.dqacc + (row0 + (size_t)r) * HD + half * 32;
+          if (deterministic && rank == 0) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+              reinterpret_cast<float4*>(base)[m] =
+                  make_float4(val[4 * m], val[4 * m + 1], val[4 * m + 2], val[4 * m + 3]);
+          } else {
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+              red_add_v4_f32(base + 4 * m, val[4 * m], val[4 * m + 1], val[4 * m + 2], val[4 * m + 3]);
+          }
+        }
+        if (deterministic) {
+          // Publish: every reducer's adds are ordered before the release of
+          // rank + 1 (fence per thread, then the barrier, then the leader's
+          // release store).
+          fence_acq_rel_gpu();
+          named_bar_sync(kReducerBar, kNumReducerThreads);
+          if (leader) st_release_gpu(sem, (uint32_t)rank + 1u);
+        }
+        ++s;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace
+
+template <int HD>
+int bwd_smem_bytes() {
+  return Cfg<HD>::kSmemBytes;
+}
+
+template <int HD>
+const void* bwd_kernel_ptr() {
+  return reinterpret_cast<const void*>(&bwd_kernel<HD>);
+}
+
+template int bwd_smem_bytes<64>();
+template int bwd_smem_bytes<128>();
+template const void* bwd_kernel_ptr<64>();
+template const void* bwd_kernel_ptr<128>();
+
+}  // namespace dab

@@ -1,0 +1,276 @@
+// fwd.cu -- attention forward for GB300 (sm_103a): O = softmax(scale Q K^T) V
+// and LSE, the inputs the backward pass consumes.
+//
+// One CTA per (head, 128-row Q tile), two passes over the visible KV tiles:
+//   pass 1: S = Q K_c^T on the tensor cores, row maximum and row sum of
+//           exp2(scale*log2(e) S - m) per Q row (online update) -> LSE;
+//   pass 2: S again, P = exp2(scale*log2(e) S - LSE*log2(e)) in bf16 written
+//           to tensor memory, O += P V_c on the tensor cores.
+// Recomputing S once avoids rescaling the O accumulator; this kernel only
+// prepares the backward's inputs, so simplicity wins over its speed.
+// Warps: 0 TMA producer, 1 MMA issuer, 2-5 softmax (thread = Q row).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tile_sched.h"
+
+namespace dab {
+
+__device__ WsHeader g_fwd_status;  // status word when the caller gives no workspace
+
+namespace {
+
+constexpr int kFwdThreads = 192;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int HD>
+struct FCfg {
+  static constexpr int kTileBytes = kTile * HD * 2;
+  static constexpr int kBlockBytes = kTile * 128;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kTileBytes;       // 2 stages
+  static constexpr int kOffV = 3 * kTileBytes;   // 2 stages
+  static constexpr int kOffBar = 5 * kTileBytes;
+  static constexpr int kOffMisc = kOffBar + 128;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColP = 128;
+  static constexpr uint32_t kColO = 256;
+  static constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);   // S = Q K^T
+  static constexpr uint32_t kIdO = idesc_bf16(128, HD, 0, 1);    // O += P V
+};
+
+struct FBars {
+  uint64_t q_full;
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full, s_free, p_full, o_done, o_full, drain;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p,
+                                                           WsHeader* hdr) {
+  using C = FCfg<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  FBars* bars = reinterpret_cast<FBars*>(smem + C::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  int* abort_flag = reinterpret_cast<int*>(smem + C::kOffMisc + 4);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (hdr == nullptr) hdr = &g_fwd_status;
+  if ((sbase & 1023u) != 0u) {
+    if (threadIdx.x == 0) raise_error(hdr, kStatusBounds, kDetailAlign);
+    return;
+  }
+  const int bh = blockIdx.x / p.N, qi = blockIdx.x % p.N;
+  const int nkv = (p.mask == kMaskCausal) ? qi + 1 : p.N;
+  const unsigned long long timeout = 2000000000ull;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 4);
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const WaitCtl wc{abort_flag, hdr, timeout};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tensormap(&p.tm_q);
+      prefetch_tensormap(&p.tm_k);
+      prefetch_tensormap(&p.tm_v);
+      mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
+      const int qrow = bh * p.S + qi * kTile;
+#pragma unroll
+      for (int db = 0; db < HD / 64; ++db)
+        tma_load_2d(smem + C::kOffQ + db * C::kBlockBytes, &p.tm_q, &bars->q_full, db * 64, qrow);
+      int it = 0, issued[2] = {0, 0};
+      bool ok = true;
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        for (int c = 0; c < nkv; ++c) {
+          const int st = it & 1;
+          if (it >= 2 && !mbar_wait(&bars->kv_empty[st], ((it >> 1) - 1) & 1, wc, 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->kv_full[st], (pass == 0 ? 1 : 2) * C::kTileBytes);
+          const int krow = bh * p.S + c * kTile;
+#pragma unroll
+          for (int db = 0; db < HD / 64; ++db) {
+            tma_load_2d(smem + C::kOffK + st * C::kTileBytes + db * C::kBlockBytes, &p.tm_k,
+                        &bars->kv_full[st], db * 64, krow);
+            if (pass == 1)
+              tma_load_2d(smem + C::kOffV + st * C::kTileBytes + db * C::kBlockBytes, &p.tm_v,
+                          &bars->kv_full[st], db * 64, krow);
+          }
+          ++issued[st];
+          ++it;
+        }
+      }
+      drain_wait(&bars->q_full, 0, hdr, timeout, 11);
+      for (int st = 0; st < 2; ++st)
+        if (issued[st] > 0) drain_wait(&bars->kv_full[st], (issued[st] - 1) & 1, hdr, timeout, 12);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t sQ = sbase + C::kOffQ;
+      bool ok = mbar_wait(&bars->q_full, 0, wc, 20);
+      int it = 0, it2 = 0;
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        for (int c = 0; c < nkv; ++c) {
+          const int st = it & 1;
+          const uint32_t sK = sbase + C::kOffK + st * C::kTileBytes;
+          const uint32_t sV = sbase + C::kOffV + st * C::kTileBytes;
+          if (!mbar_wait(&bars->kv_full[st], (it >> 1) & 1, wc, 21)) { ok = false; break; }
+          if (it > 0 && !mbar_wait(&bars->s_free, (it - 1) & 1, wc, 22)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < HD / 16; ++k)
+            mma_ss(tbase + C::kColS, desc_kmajor(sQ, k, 128), desc_kmajor(sK, k, 128), C::kIdS, k > 0);
+          mma_commit(&bars->s_full);
+          if (pass == 0) {
+            mma_commit(&bars->kv_empty[st]);
+          } else {
+            if (!mbar_wait(&bars->p_full, it2 & 1, wc, 23)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kTile / 16; ++k)
+              mma_ts(tbase + C::kColO, tbase + C::kColP + 8 * k, desc_mnmajor(sV, k, 128), C::kIdO,
+                     !(c == 0 && k == 0));
+            mma_commit(&bars->o_done);
+            mma_commit(&bars->kv_empty[st]);
+            ++it2;
+          }
+          ++it;
+        }
+      }
+      if (ok) mma_commit(&bars->o_full);
+      mma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0, hdr, timeout, 13);
+    }
+    __syncwarp();
+  } else {
+    // softmax warps 2..5; thread = Q row r of the tile
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const bool causal = (p.mask == kMaskCausal);
+    float m = -INFINITY, l = 0.f;
+    int it = 0;
+    bool ok = true;
+    for (int c = 0; c < nkv && ok; ++c, ++it) {
+      if (!warp_wait(&bars->s_full, it & 1, wc, 30)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_off + C::kColS + 32 * ch, v);
+        float x[32];
+        float cmax = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = 32 * ch + e;
+          x[e] = __uint_as_float(v[e]) * p.scale_log2e;
+          if (causal && c == qi && col > r) x[e] = -INFINITY;
+          cmax = fmaxf(cmax, x[e]);
+        }
+        const float mn = fmaxf(m, cmax);
+        float sum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sum += ex2_approx(x[e] - mn);
+        l = l * ex2_approx(m - mn) + sum;
+        m = mn;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_free);
+    }
+    const float lse2 = m + __log2f(l);
+    for (int c = 0, it2 = 0; c < nkv && ok; ++c, ++it, ++it2) {
+      if (!warp_wait(&bars->s_full, it & 1, wc, 31)) { ok = false; break; }
+      if (it2 > 0 && !warp_wait(&bars->o_done, (it2 - 1) & 1, wc, 32)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_off + C::kColS + 32 * ch, v);
+        uint32_t w16[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int col = 32 * ch + e;
+          float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2e, -lse2));
+          float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2e, -lse2));
+          if (causal && c == qi) {
+            if (col > r) p0 = 0.f;
+            if (col + 1 > r) p1 = 0.f;
+          }
+          w16[e >> 1] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tbase + lane_off + C::kColP + 16 * ch, w16);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars->s_free);
+        mbar_arrive(&bars->p_full);
+      }
+    }
+    if (ok && warp_wait(&bars->o_full, 0, wc, 33)) {
+      tc_fence_after();
+      const size_t row = (size_t)bh * p.S + (size_t)qi * kTile + r;
+#pragma unroll
+      for (int ch = 0; ch < HD / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_off + C::kColO + 32 * ch, v);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + row * HD + 32 * ch);
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm)
+          dst[mm] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * mm]), __uint_as_float(v[8 * mm + 1])),
+                               pack_bf16x2(__uint_as_float(v[8 * mm + 2]), __uint_as_float(v[8 * mm + 3])),
+                               pack_bf16x2(__uint_as_float(v[8 * mm + 4]), __uint_as_float(v[8 * mm + 5])),
+                               pack_bf16x2(__uint_as_float(v[8 * mm + 6]), __uint_as_float(v[8 * mm + 7])));
+      }
+      p.lse[row] = lse2 * kLn2;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace
+
+template <int HD>
+int fwd_smem_bytes() {
+  return FCfg<HD>::kSmemBytes;
+}
+template <int HD>
+const void* fwd_kernel_ptr() {
+  return reinterpret_cast<const void*>(&fwd_kernel<HD>);
+}
+template int fwd_smem_bytes<64>();
+template int fwd_smem_bytes<128>();
+template const void* fwd_kernel_ptr<64>();
+template const void* fwd_kernel_ptr<128>();
+
+}  // namespace dab

@@ -1,0 +1,219 @@
+/*
+ * dab.h -- C ABI of the deterministic attention backward library (libdab.so)
+ * for GB300 (sm_103a).
+ *
+ * The operation: exact softmax attention O = softmax(scale * Q K^T, mask) V
+ * and its backward pass, which produces dQ, dK and dV with the dQ partial
+ * sums of all KV tiles added in a fixed order, so that the deterministic
+ * schedules give bitwise-identical gradients from run to run.  The schedules
+ * are those of "DASH: Deterministic Attention Scheduling for High-throughput
+ * Reproducible LLM Training" (arXiv 2601.21824): the serialised baseline
+ * (technical summary section 1), Descending Q-Tile Iteration (section 2.2.A)
+ * and Shift Scheduling, with the symmetric variant for causal masks
+ * (section 2.2.B), plus the non-deterministic atomic counterpart that the
+ * abstract compares against.
+ *
+ * Conventions shared by every entry point
+ *   Layout   Q, K, V, O, dO, dQ, dK, dV are contiguous bfloat16 tensors of
+ *            shape [B][H][S][d] (row-major, d innermost); LSE is a contiguous
+ *            float32 tensor [B][H][S] holding the natural log of
+ *            sum_c exp(scale * q_r . k_c) over the visible keys.  Query and key
+ *            sequences have the same length S.
+ *   Shapes   d must be 64 or 128; S must be a positive multiple of 128;
+ *            B, H >= 1; B*H*S < 2^31.
+ *   Mask     DAB_MASK_CAUSAL hides key c from query r when c > r (the diagonal
+ *            is visible, so no query row is empty).
+ *   Memory   Every pointer is a device pointer, allocated and owned by the
+ *            caller, 16-byte aligned.  The library allocates no device memory
+ *            and keeps no state between calls except a per-device cache of
+ *            kernel attributes.
+ *   Streams  Every call is asynchronous on `stream` and may run concurrently
+ *            with calls on other streams that use distinct workspaces.
+ *   Errors   Argument errors are returned synchronously and launch nothing.
+ *            DAB_ERR_CUDA reports a failed kernel launch.  Faults detected on
+ *            the device (a bounded wait that ran out, an index out of range)
+ *            never trap: the kernels record them in the workspace status word
+ *            and return, and dab_check_status() reports them.
+ */
+#ifndef DAB_H_
+#define DAB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DAB_MASK_FULL = 0,
+    DAB_MASK_CAUSAL = 1
+} dab_mask_t;
+
+/* Backward schedules.
+ *   SERIAL        KV tile i walks its Q tiles in ascending order; dQ_j gathers
+ *                 its partial sums in ascending KV order (rank(i, j) = i).
+ *                 The serialised deterministic baseline (DASH summary sec. 1).
+ *   DESCENDING_Q  Same reduction order as SERIAL, Q tiles walked from the last
+ *                 one down (DASH summary sec. 2.2.A).  Bitwise equal to SERIAL.
+ *   SHIFT         Full mask: KV tile i walks Q tiles i, i+1, ..., N-1, 0, ...,
+ *                 i-1 and dQ_j is reduced in visit order (DASH summary
+ *                 sec. 2.2.B).  Causal mask: the symmetric variant, where one
+ *                 CTA handles KV tiles p and N-1-p in a dense phase and a
+ *                 folded phase; needs an even number of tiles N = S/128.
+ *   ATOMIC        Unordered float atomics; the only schedule whose bits may
+ *                 differ between runs (the non-deterministic counterpart).   */
+typedef enum {
+    DAB_SCHED_SERIAL = 0,
+    DAB_SCHED_DESCENDING_Q = 1,
+    DAB_SCHED_SHIFT = 2,
+    DAB_SCHED_ATOMIC = 3
+} dab_sched_t;
+
+typedef enum {
+    DAB_OK = 0,
+    DAB_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad shape or enum */
+    DAB_ERR_UNSUPPORTED = 2,   /* valid but not supported here (e.g. odd N for
+                                  causal SHIFT, no sm_100-family device)     */
+    DAB_ERR_WORKSPACE = 3,     /* workspace missing or too small             */
+    DAB_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed       */
+    DAB_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out             */
+    DAB_ERR_DEVICE_BOUNDS = 6  /* device: an index or alignment check failed */
+} dab_status_t;
+
+/* Attention forward: writes O (bf16 [B][H][S][d]) and LSE (f32 [B][H][S]).
+ * Produces the O and LSE that the backward consumes.  `workspace` is unused
+ * and may be NULL (ws_bytes 0).                                              */
+dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v,
+                          void* o, float* lse,
+                          int B, int H, int S, int d, float scale,
+                          dab_mask_t mask,
+                          void* workspace, size_t ws_bytes,
+                          cudaStream_t stream);
+
+/* Bytes of device workspace that dab_attn_bwd needs for this problem (0 on
+ * invalid arguments).  The workspace holds the status word, the dispatch
+ * counter, one semaphore per 128-row dQ tile, D and LSE*log2(e) per row, and
+ * the float32 dQ accumulator [B][H][S][d].  It needs no initialisation: the
+ * first kernel of every backward call resets what must start at zero.      */
+size_t dab_bwd_workspace_size(int B, int H, int S, int d,
+                              dab_mask_t mask, dab_sched_t sched);
+
+/* Attention backward.  Inputs Q, K, V, O, dO (bf16) and LSE (f32) as produced
+ * by dab_attn_fwd; outputs dQ, dK, dV (bf16), each written in full.
+ * Launches, on `stream`:
+ *   1. the preprocess kernel: D_r = sum_k dO_rk O_rk (f32), LSE*log2(e),
+ *      reset of the semaphores, status word and dispatch counter (and, for
+ *      ATOMIC, zeroing of the dQ accumulator);
+ *   2. the persistent main kernel: per KV tile, S, P, dV, dP, dS, dK and the
+ *      dQ partial on the tensor cores, then the dQ reduction in the order
+ *      `sched` defines (semaphore-ordered, no float atomics, for the three
+ *      deterministic schedules);
+ *   3. the convert kernel: dQ = bf16(scale * dQacc).
+ * The call returns once the kernels are queued.                              */
+dab_status_t dab_attn_bwd(const void* q, const void* k, const void* v,
+                          const void* o, const float* lse, const void* dout,
+                          void* dq, void* dk, void* dv,
+                          int B, int H, int S, int d, float scale,
+                          dab_mask_t mask, dab_sched_t sched,
+                          void* workspace, size_t ws_bytes,
+                          cudaStream_t stream);
+
+/* Synchronises `stream`, then reads the status word that the backward kernels
+ * of the last call on this workspace wrote.  Returns DAB_OK, DAB_ERR_TIMEOUT
+ * or DAB_ERR_DEVICE_BOUNDS (or DAB_ERR_CUDA if the synchronisation failed).  */
+dab_status_t dab_check_status(const void* workspace, cudaStream_t stream);
+
+/* Static, human-readable name of a status code.                             */
+const char* dab_status_string(dab_status_t status);
+
+/* ------------------------------------------------------------------------ */
+/* Extended backward options.  dab_attn_bwd() is dab_attn_bwd_ex() with
+ * opts == NULL.                                                              */
+typedef struct {
+    uint64_t spin_timeout_ns; /* limit of every device-side wait; 0 = default
+                                 (2 s)                                         */
+    uint32_t flags;           /* DAB_BWD_* bits below                         */
+    int32_t grid;             /* CTAs of the main kernel; 0 = one per SM      */
+} dab_bwd_opts_t;
+
+/* Skip the preprocess kernel: the caller has run dab_bwd_preprocess() on this
+ * workspace itself (used to inject faults from the host, e.g. to poison a
+ * semaphore and check that the bounded wait reports DAB_ERR_TIMEOUT).       */
+#define DAB_BWD_SKIP_PREPROCESS 0x1u
+/* Skip the convert kernel (dQ is left in the workspace accumulator).        */
+#define DAB_BWD_SKIP_CONVERT 0x2u
+
+dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v,
+                             const void* o, const float* lse, const void* dout,
+                             void* dq, void* dk, void* dv,
+                             int B, int H, int S, int d, float scale,
+                             dab_mask_t mask, dab_sched_t sched,
+                             void* workspace, size_t ws_bytes,
+                             cudaStream_t stream, const dab_bwd_opts_t* opts);
+
+/* The preprocess step alone (step 1 of dab_attn_bwd), for the flag above.   */
+dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dout,
+                                int B, int H, int S, int d,
+                                dab_mask_t mask, dab_sched_t sched,
+                                void* workspace, size_t ws_bytes,
+                                cudaStream_t stream);
+
+/* Byte offsets of the workspace regions (for tests and tools).             */
+typedef struct {
+    size_t status;   /* uint32 status word, uint32 error detail, uint32 counter */
+    size_t sem;      /* uint32 [B*H][N] semaphores                              */
+    size_t D;        /* float  [B*H*S]                                          */
+    size_t lse2;     /* float  [B*H*S] LSE * log2(e)                            */
+    size_t dqacc;    /* float  [B*H*S][d]                                       */
+    size_t total;
+} dab_ws_layout_t;
+
+dab_status_t dab_bwd_workspace_layout(int B, int H, int S, int d,
+                                      dab_mask_t mask, dab_sched_t sched,
+                                      dab_ws_layout_t* layout);
+
+/* ------------------------------------------------------------------------ */
+/* Schedule introspection (host only, no GPU needed).  N = S/128 tiles.
+ * These are the same functions the main kernel evaluates on the device.     */
+
+/* Work units per head: N, or N/2 for causal SHIFT (one unit = a KV pair).   */
+int dab_sched_units_per_head(dab_sched_t sched, dab_mask_t mask, int N);
+/* Steps (KV tile, Q tile) of unit u, in execution order.                    */
+int dab_sched_unit_steps(dab_sched_t sched, dab_mask_t mask, int N, int u);
+/* Step t of unit u: its KV tile i and Q tile j.  Returns 0, or -1 if out of
+ * range.                                                                     */
+int dab_sched_step(dab_sched_t sched, dab_mask_t mask, int N, int u, int t,
+                   int* kv_tile, int* q_tile);
+/* rank(i, j): the position of KV tile i in dQ_j's fixed reduction order
+ * (0 = first), -1 if tile (i, j) is masked out or for ATOMIC.              */
+int dab_sched_rank(dab_sched_t sched, dab_mask_t mask, int N, int i, int j);
+/* Number of KV tiles that contribute to dQ_j.                               */
+int dab_sched_contributors(dab_mask_t mask, int N, int j);
+/* Units that must run at the same time for progress (1 when none must).     */
+int dab_sched_gang_size(dab_sched_t sched, dab_mask_t mask, int N);
+
+/* DAG model of one schedule (DASH summary sec. 2.1): a node per (KV tile,
+ * Q tile) step made of a compute phase of weight wc and a reduction phase of
+ * weight wr; edges are the KV-chain order and the dQ_j reduction order.
+ * `reducer_depth` = 0 runs the reduction inside the chain (the next compute
+ * waits for it); k > 0 lets up to k reductions trail the compute phases.
+ * `heads` heads run on `ctas` processors that take units in dispatch order.
+ * Outputs the makespan and the busy fraction (sum of weights / (ctas *
+ * makespan)).  Returns 0, -1 on bad arguments, -2 if the units deadlock
+ * (a gang that cannot be co-resident).                                      */
+int dab_dag_simulate(dab_sched_t sched, dab_mask_t mask, int N, int heads,
+                     int ctas, double wc, double wr, int reducer_depth,
+                     double* makespan, double* busy_fraction);
+
+/* Longest path of one head's DAG with one processor per unit.               */
+double dab_dag_critical_path(dab_sched_t sched, dab_mask_t mask, int N,
+                             double wc, double wr, int reducer_depth);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DAB_H_ */

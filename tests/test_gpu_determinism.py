@@ -1,0 +1,41 @@
+"""Bitwise run-to-run reproducibility of the deterministic schedules."""
+import pytest
+import torch
+
+import deterministic_attn_backward_gb300 as dab
+from gpu_common import case
+
+RUNS = 20
+
+
+def _grads(B, H, S, d, mask, sched, runs):
+    q, k, v, do = (t.cuda() for t in case(B, H, S, d, 11))
+    o, lse = dab.attn_fwd(q, k, v, mask)
+    ws = dab.new_workspace(B, H, S, d, mask, sched)
+    out = []
+    for _ in range(runs):
+        g = dab.attn_bwd(q, k, v, o, lse, do, mask, sched, workspace=ws)
+        out.append(tuple(t.clone() for t in g))
+    assert dab.check_status(ws) == 0
+    return out
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ["full", "causal"])
+@pytest.mark.parametrize("sched", ["serial", "descending_q", "shift"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bitwise_repeatable(mask, sched, d):
+    runs = _grads(2, 4, 1024, d, mask, sched, RUNS)
+    for r in runs[1:]:
+        for a, b in zip(runs[0], r):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ["full", "causal"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_descending_equals_serial_bitwise(mask, d):
+    a = _grads(2, 4, 1024, d, mask, "serial", 1)[0]
+    b = _grads(2, 4, 1024, d, mask, "descending_q", 1)[0]
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
