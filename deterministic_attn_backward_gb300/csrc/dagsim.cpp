@@ -13,7 +13,7 @@
 // Edges:
 //   C(U,t-1) -> C(U,t)                       (the CTA computes in order)
 //   R(U,t-1) -> C(U,t)      reducer_depth 0   (reduction inside the chain)
-//   R(U,t-k) -> C(U,t)      reducer_depth k   (k reductions may trail)
+//   R(U,t-1-k) -> C(U,t)    reducer_depth k   (k reductions may trail)
 //   C(U,t) -> R(U,t),  R(U,t-1) -> R(U,t)     (one reducer per CTA)
 //   R(rank-1 contributor of dQ_j) -> R(U,t)   (fixed reduction order)
 //   last C / R of the previous unit on the same CTA -> first C / R of U.
@@ -102,7 +102,7 @@ bool run_static(const Problem& P, double* makespan) {
       if (t > 0) {
         edge(2 * (n - 1), 2 * n);
         edge(2 * (n - 1) + 1, 2 * n + 1);
-        const int k = P.reducer_depth == 0 ? 1 : P.reducer_depth;
+        const int k = P.reducer_depth + 1;  // C(t) waits for R(t - 1 - depth)
         if (t - k >= 0) edge(2 * (n - k) + 1, 2 * n);
       }
       edge(2 * n, 2 * n + 1);
@@ -156,7 +156,7 @@ bool run_dynamic(const Problem& P, double* makespan) {
       const int n = base + t;
       double cs = cprev;
       if (t > 0) {
-        const int k = P.reducer_depth == 0 ? 1 : P.reducer_depth;
+        const int k = P.reducer_depth + 1;
         if (t - k >= 0) cs = std::max(cs, r_fin[n - k]);
       }
       c_fin[n] = cs + P.wc;

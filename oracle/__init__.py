@@ -60,6 +60,11 @@ def _declare(lib):
     lib.oracle_attn_bwd_given.argtypes = (
         [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int]
         + [dp] * 6 + [dp] * 6 + [ctypes.c_int])
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.oracle_attn_rows.restype = ctypes.c_int
+    lib.oracle_attn_rows.argtypes = (
+        [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int] + [dp] * 6
+        + [ip, ctypes.c_int, ip, ctypes.c_int] + [dp] * 6 + [ctypes.c_int])
     return lib
 
 
@@ -126,4 +131,31 @@ def attn_bwd_given(q, k, v, o, lse, dout, scale: float, causal: bool,
         int(nthreads or default_threads()))
     if rc != 0:
         raise RuntimeError(f"oracle_attn_bwd_given failed ({rc})")
+    return out
+
+
+def attn_rows(q, k, v, dout, scale: float, causal: bool, qrows, krows,
+              lse_all=None, D_all=None, nthreads: int | None = None, lib=None) -> dict:
+    """Selected rows of one head ([S, d] inputs): O, LSE, D, dQ for `qrows`,
+    dK, dV for `krows`.  `lse_all`/`D_all` ([S], from a whole-head run) skip
+    the whole-head query pass that the key rows otherwise need."""
+    lib = lib or load()
+    q, k, v, dout = (_f64(t) for t in (q, k, v, dout))
+    S, d = q.shape
+    qr = np.ascontiguousarray(np.asarray(qrows, dtype=np.int32))
+    kr = np.ascontiguousarray(np.asarray(krows, dtype=np.int32))
+    nq, nk = len(qr), len(kr)
+    out = {"o": np.empty((nq, d)), "lse": np.empty(nq), "D": np.empty(nq),
+           "dq": np.empty((nq, d)), "dk": np.empty((nk, d)), "dv": np.empty((nk, d))}
+    la = _f64(lse_all) if lse_all is not None else None
+    da = _f64(D_all) if D_all is not None else None
+    ip = ctypes.POINTER(ctypes.c_int)
+    rc = lib.oracle_attn_rows(
+        S, d, float(scale), int(bool(causal)), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+        _ptr(la) if la is not None else None, _ptr(da) if da is not None else None,
+        qr.ctypes.data_as(ip), nq, kr.ctypes.data_as(ip), nk,
+        _ptr(out["o"]), _ptr(out["lse"]), _ptr(out["D"]), _ptr(out["dq"]),
+        _ptr(out["dk"]), _ptr(out["dv"]), int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_rows failed ({rc})")
     return out

@@ -59,7 +59,9 @@ typedef struct {
 typedef struct {
     head_job *job;
     int tid, nthreads;
-    int phase; /* 1: query rows, 2: key rows */
+    int phase;       /* 1: query rows, 2: key rows */
+    const int *rows; /* rows to process (NULL: all S rows) */
+    int nrows;
 } worker_arg;
 
 static int is_masked(int causal, int r, int c) { return causal && c > r; }
@@ -161,20 +163,22 @@ static void *worker(void *argp)
 {
     worker_arg *a = (worker_arg *)argp;
     head_job *h = a->job;
+    const int n = a->rows ? a->nrows : h->S;
     if (a->phase == 1) {
         double *s = (double *)malloc(sizeof(double) * (size_t)h->S);
         double *p = (double *)malloc(sizeof(double) * (size_t)h->S);
         if (s == NULL || p == NULL) { free(s); free(p); return (void *)1; }
-        for (int r = a->tid; r < h->S; r += a->nthreads) query_row(h, r, s, p);
+        for (int x = a->tid; x < n; x += a->nthreads)
+            query_row(h, a->rows ? a->rows[x] : x, s, p);
         free(s);
         free(p);
     } else {
-        for (int c = a->tid; c < h->S; c += a->nthreads) key_row(h, c);
+        for (int x = a->tid; x < n; x += a->nthreads) key_row(h, a->rows ? a->rows[x] : x);
     }
     return NULL;
 }
 
-static int run_phase(head_job *h, int phase, int nthreads)
+static int run_phase_rows(head_job *h, int phase, const int *rows, int nrows, int nthreads)
 {
     pthread_t th[256];
     worker_arg args[256];
@@ -186,6 +190,8 @@ static int run_phase(head_job *h, int phase, int nthreads)
         args[t].tid = t;
         args[t].nthreads = nthreads;
         args[t].phase = phase;
+        args[t].rows = rows;
+        args[t].nrows = nrows;
         if (t > 0 && pthread_create(&th[t], NULL, worker, &args[t]) != 0) {
             /* fall back: run this share on the calling thread */
             if (worker(&args[t]) != NULL) failed = 1;
@@ -201,6 +207,11 @@ static int run_phase(head_job *h, int phase, int nthreads)
         }
     }
     return failed ? -1 : 0;
+}
+
+static int run_phase(head_job *h, int phase, int nthreads)
+{
+    return run_phase_rows(h, phase, NULL, 0, nthreads);
 }
 
 static int run_heads(int BH, int S, int d, double scale, int causal,
@@ -249,4 +260,59 @@ int oracle_attn_bwd_given(int BH, int S, int d, double scale, int causal,
     if (o_in == NULL || lse_in == NULL) return -2;
     return run_heads(BH, S, d, scale, causal, q, k, v, dout, o_in, lse_in,
                      o_out, lse_out, D, dq, dk, dv, nthreads);
+}
+
+/* Selected rows of one head [S][d].  Query rows `qrows` get steps 1-6 and
+ * 8-10 (O, LSE, D, dQ); key rows `krows` get steps 7 and 11 (dK, dV).  The
+ * key rows need LSE_r and D_r of every query row: pass them in lse_all /
+ * D_all (as a whole-head run produced them), or NULL to compute them here
+ * first (a whole-head query pass).  Outputs are [nq][d], [nq], [nq], [nq][d],
+ * [nk][d], [nk][d].                                                         */
+int oracle_attn_rows(int S, int d, double scale, int causal,
+                     const double *q, const double *k, const double *v,
+                     const double *dout, const double *lse_all, const double *D_all,
+                     const int *qrows, int nq, const int *krows, int nk,
+                     double *o_rows, double *lse_rows, double *D_rows, double *dq_rows,
+                     double *dk_rows, double *dv_rows, int nthreads)
+{
+    if (S <= 0 || d <= 0 || nq < 0 || nk < 0) return -2;
+    for (int x = 0; x < nq; ++x) if (qrows[x] < 0 || qrows[x] >= S) return -2;
+    for (int x = 0; x < nk; ++x) if (krows[x] < 0 || krows[x] >= S) return -2;
+    const size_t Sd = (size_t)S * (size_t)d;
+    double *o = (double *)calloc(Sd, sizeof(double));
+    double *dq = (double *)calloc(Sd, sizeof(double));
+    double *dk = (double *)calloc(Sd, sizeof(double));
+    double *dv = (double *)calloc(Sd, sizeof(double));
+    double *lse = (double *)calloc((size_t)S, sizeof(double));
+    double *D = (double *)calloc((size_t)S, sizeof(double));
+    int rc = 0;
+    head_job h;
+    if (!o || !dq || !dk || !dv || !lse || !D) { rc = -1; goto done; }
+    h.S = S; h.d = d; h.causal = causal; h.scale = scale;
+    h.q = q; h.k = k; h.v = v; h.dout = dout;
+    h.o_in = NULL; h.lse_in = NULL;
+    h.o = o; h.lse = lse; h.D = D; h.dq = dq; h.dk = dk; h.dv = dv;
+    if (nk > 0) {
+        if (lse_all != NULL && D_all != NULL) {
+            memcpy(lse, lse_all, sizeof(double) * (size_t)S);
+            memcpy(D, D_all, sizeof(double) * (size_t)S);
+        } else if (run_phase(&h, 1, nthreads) != 0) { rc = -1; goto done; }
+    }
+    if (nq > 0 && run_phase_rows(&h, 1, qrows, nq, nthreads) != 0) { rc = -1; goto done; }
+    if (nk > 0 && run_phase_rows(&h, 2, krows, nk, nthreads) != 0) { rc = -1; goto done; }
+    for (int x = 0; x < nq; ++x) {
+        const int r = qrows[x];
+        memcpy(o_rows + (size_t)x * d, o + (size_t)r * d, sizeof(double) * (size_t)d);
+        memcpy(dq_rows + (size_t)x * d, dq + (size_t)r * d, sizeof(double) * (size_t)d);
+        lse_rows[x] = lse[r];
+        D_rows[x] = D[r];
+    }
+    for (int x = 0; x < nk; ++x) {
+        const int c = krows[x];
+        memcpy(dk_rows + (size_t)x * d, dk + (size_t)c * d, sizeof(double) * (size_t)d);
+        memcpy(dv_rows + (size_t)x * d, dv + (size_t)c * d, sizeof(double) * (size_t)d);
+    }
+done:
+    free(o); free(dq); free(dk); free(dv); free(lse); free(D);
+    return rc;
 }

@@ -1,0 +1,85 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments synchronously (no GPU needed: no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import deterministic_attn_backward_gb300 as dab
+
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(INCLUDE):
+        if not fn.endswith(".h"):
+            continue
+        with open(os.path.join(INCLUDE, fn)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(dab_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from deterministic_attn_backward_gb300 import build
+    build.build()
+    return dab.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(dab.EXPORTED)
+
+
+def test_status_strings(lib):
+    for code, name in dab.STATUS.items():
+        assert lib.dab_status_string(code).decode() == name
+
+
+def test_workspace_layout(lib):
+    B, H, S, d = 2, 16, 8192, 128
+    L = dab.workspace_layout(B, H, S, d, "causal", "descending_q")
+    rows = B * H * S
+    assert L.status == 0 and L.sem == 256
+    assert L.D >= L.sem + 4 * B * H * (S // 128)
+    assert L.lse2 >= L.D + 4 * rows and L.dqacc >= L.lse2 + 4 * rows
+    assert L.total >= L.dqacc + 4 * rows * d
+    for off in (L.sem, L.D, L.lse2, L.dqacc, L.total):
+        assert off % 256 == 0
+    assert dab.workspace_size(B, H, S, d) == L.total
+    assert lib.dab_bwd_workspace_size(B, H, 100, d, 0, 0) == 0      # S not a multiple of 128
+    assert lib.dab_bwd_workspace_size(B, H, S, 96, 0, 0) == 0       # d not 64/128
+    assert lib.dab_bwd_workspace_size(B, H, S, d, 2, 0) == 0        # bad mask
+
+
+def test_bad_arguments_rejected_without_touching_the_device(lib):
+    p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    nul = None
+    big = 1 << 30
+    call = lambda *a: lib.dab_attn_bwd(*a)
+    # null / misaligned pointers
+    assert call(nul, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, p, big, None) == 1
+    assert call(ctypes.c_void_p(17), p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, p, big,
+                None) == 1
+    # bad shape / enum / scale
+    assert call(p, p, p, p, p, p, p, p, p, 1, 1, 192, 64, 0.125, 0, 0, p, big, None) == 1
+    assert call(p, p, p, p, p, p, p, p, p, 1, 1, 128, 80, 0.125, 0, 0, p, big, None) == 1
+    assert call(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 7, p, big, None) == 1
+    assert call(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, -1.0, 0, 0, p, big, None) == 1
+    # causal shift with an odd tile count
+    assert call(p, p, p, p, p, p, p, p, p, 1, 1, 384, 64, 0.125, 1, 2, p, big, None) == 2
+    # workspace missing or too small
+    assert call(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, nul, 0, None) == 3
+    assert call(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, p, 64, None) == 3
+    # forward
+    assert lib.dab_attn_fwd(nul, p, p, p, p, 1, 1, 128, 64, 0.125, 0, nul, 0, None) == 1
+    assert lib.dab_attn_fwd(p, p, p, p, p, 1, 1, 128, 64, 0.125, 3, nul, 0, None) == 1
+    assert lib.dab_check_status(nul, None) == 1

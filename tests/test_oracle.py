@@ -33,3 +33,18 @@ def test_given_mode_matches_full_mode(lib):
         b = oracle.attn_bwd_given(q, k, v, a["o"], a["lse"], do, 0.5, causal, lib=lib)
         for n in ("D", "dq", "dk", "dv"):
             assert np.allclose(a[n], b[n], rtol=0, atol=1e-13), n
+
+
+def test_row_sampled_mode_matches_whole_head(lib):
+    rng = np.random.default_rng(8)
+    q, k, v, do = (rng.standard_normal((40, 8)) for _ in range(4))
+    qrows, krows = [0, 7, 39, 13], [39, 0, 22]
+    for causal in (False, True):
+        full = oracle.attn_fwd_bwd(q[None], k[None], v[None], do[None], 0.4, causal, lib=lib)
+        for given in (False, True):
+            kw = dict(lse_all=full["lse"][0], D_all=full["D"][0]) if given else {}
+            part = oracle.attn_rows(q, k, v, do, 0.4, causal, qrows, krows, lib=lib, **kw)
+            for n in ("o", "lse", "D", "dq"):
+                assert np.array_equal(part[n], full[n][0][qrows]), n
+            for n in ("dk", "dv"):
+                assert np.array_equal(part[n], full[n][0][krows]), n
