@@ -1,0 +1,403 @@
+"""Benchmark: deterministic attention backward TFLOP/s on GB300.
+
+One step = one pass of the whole backward hot path (preprocess, main kernel,
+dQ convert) over the workload B=2, H=16, S=8192, d=128 with the causal mask
+(Q and K scaled by 0.5, seed 2) and again with the full mask at the same
+shape, each with its deterministic schedule.  FLOPs: 10*B*H*S^2*d for the full
+mask, half for causal (exp, preprocess and convert not counted).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `--impl reference` times the float64 CPU oracle on the
+host cores on bounded row samples of the same workload.  Under torchrun each
+rank runs its own replica (the path does not shard); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "deterministic attn-bwd TFLOP/s (causal+full) and % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+B, H, S, D = 2, 16, 8192, 128
+SEED, QK_SCALE = 2, 0.5
+STEP_SCHEDS = {"causal": "descending_q", "full": "shift"}  # the schedules one step runs
+ALL_SCHEDS = ("serial", "descending_q", "shift", "atomic")
+MASKS = ("causal", "full")
+
+
+def flops(mask: str) -> float:
+    f = 10.0 * B * H * S * S * D
+    return f if mask == "full" else f / 2.0
+
+
+def workload_name() -> str:
+    return f"attn_bwd_b{B}h{H}s{S}d{D}_causal+full"
+
+
+def load_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]), "hbm_gbs": float(p["hbm_gbs"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Maximum of a per-rank float over the process group (identity at N=1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+    import deterministic_attn_backward_gb300 as dab
+    from deterministic_attn_backward_gb300 import inputs
+
+    dab.load_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    q, k, v, do = inputs.make_qkvdo(B, H, S, D, SEED, QK_SCALE)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    fwd = {m: dab.attn_fwd(qd, kd, vd, m) for m in MASKS}
+    ws = {m: dab.new_workspace(B, H, S, D, m, "atomic", dev) for m in MASKS}
+    outs = {m: tuple(torch.empty_like(qd) for _ in range(3)) for m in MASKS}
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def bwd(mask, sched):
+        o, lse = fwd[mask]
+        dab.attn_bwd(qd, kd, vd, o, lse, dod, mask, sched, workspace=ws[mask], out=outs[mask])
+
+    def step():
+        for m in MASKS:
+            bwd(m, STEP_SCHEDS[m])
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def check():
+        for m in MASKS:
+            st = dab.check_status(ws[m])
+            if st != 0:
+                raise RuntimeError(f"device status {st} ({m})")
+
+    step()
+    check()
+
+    # ---- per-schedule table: device time per call of the whole hot path
+    per = {}
+    for m in MASKS:
+        per[m] = {}
+        for sched in ALL_SCHEDS:
+            for _ in range(3):
+                bwd(m, sched)
+            torch.cuda.synchronize(dev)
+            reps = 10
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            for _ in range(reps):
+                bwd(m, sched)
+            e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            per[m][sched] = {"ms": round(ms, 4), "tflops": round(flops(m) / ms / 1e9, 2)}
+        check()
+        ts, ta = per[m]["serial"]["ms"], per[m]["atomic"]["ms"]
+        for sched in ("descending_q", "shift"):
+            gap = ts - ta
+            per[m][sched]["gap_closure"] = (round((ts - per[m][sched]["ms"]) / gap, 3)
+                                            if abs(gap) > 1e-9 else None)
+
+    # ---- the dominant kernel alone (events around each main-kernel launch)
+    opts = dab.BwdOpts(spin_timeout_ns=0,
+                       flags=dab.DAB_BWD_SKIP_PREPROCESS | dab.DAB_BWD_SKIP_CONVERT, grid=0)
+    main_ms = {}
+    for m in MASKS:
+        o, lse = fwd[m]
+        sched = STEP_SCHEDS[m]
+        tot, reps = 0.0, 10
+        for it in range(reps + 3):
+            dab.bwd_preprocess(o, lse, dod, m, sched, ws[m])
+            a, b_ = ev(), ev()
+            a.record(stream)
+            dab.attn_bwd(qd, kd, vd, o, lse, dod, m, sched, workspace=ws[m], out=outs[m], opts=opts)
+            b_.record(stream)
+            b_.synchronize()
+            if it >= 3:
+                tot += a.elapsed_time(b_)
+        main_ms[m] = tot / reps
+    check()
+
+    # ---- the timed region
+    for _ in range(args.warmup):
+        step()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    clocks = sampler.stop() if sampler else None
+    check()
+    ms_total = max_over_ranks(ms_total, world, dev)
+
+    # ---- end to end: host buffers through the public API, copies in the timed region
+    host_in = {m: tuple(t.cpu().pin_memory() for t in (q, k, v, fwd[m][0], fwd[m][1], do))
+               for m in MASKS}
+    host_out = {m: tuple(torch.empty_like(q).pin_memory() for _ in range(3)) for m in MASKS}
+    dev_in = {m: tuple(torch.empty_like(t, device=dev) for t in host_in[m]) for m in MASKS}
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for m in MASKS:
+            for hd, dd in zip(host_in[m], dev_in[m]):
+                dd.copy_(hd, non_blocking=True)
+            qq, kk, vv, oo, ll, gg = dev_in[m]
+            dab.attn_bwd(qq, kk, vv, oo, ll, gg, m, STEP_SCHEDS[m], workspace=ws[m], out=outs[m])
+            for dd, hh in zip(outs[m], host_out[m]):
+                hh.copy_(dd, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    c0, c1 = ev(), ev()
+    c0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    c1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(c0.elapsed_time(c1), world, dev) / e2e_steps
+    check()
+    h2d = sum(t.numel() * t.element_size() for m in MASKS for t in host_in[m])
+    d2h = sum(t.numel() * t.element_size() for m in MASKS for t in host_out[m])
+
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    step_flops = flops("causal") + flops("full")
+    ms_step = ms_total / args.steps
+    value = world * step_flops / (ms_step * 1e9)
+    main_avg = (main_ms["causal"] + main_ms["full"]) / 2.0
+    achieved = step_flops / 2.0 / main_avg / 1e9   # algorithmic FLOPs per launch / launch time
+    peak = peaks["bf16_tflops"]
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": workload_name(), "B": B, "H": H, "S": S, "d": D,
+                   "masks": list(MASKS), "schedules": STEP_SCHEDS, "seed": SEED,
+                   "qk_scale": QK_SCALE,
+                   "l2": "inputs exceed L2 (5 x 64 MiB read per call), no flush",
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_peak": round(value / world / peak, 4),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "bwd_kernel<128>", "peak_source": peaks["source"] + " (burst)",
+                     "launch_ms": {m: round(x, 4) for m, x in main_ms.items()}},
+        "per_schedule": per,
+        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e9), 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 6 * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu_baseline(),
+    }
+
+
+# ---------------------------------------------------------------- oracle
+def _oracle_head_time(q, k, v, do, b, h, mask, lib, threads):
+    import oracle
+    args = [t[b, h].unsqueeze(0) for t in (q, k, v, do)]
+    t0 = time.perf_counter()
+    out = oracle.attn_fwd_bwd(*args, 1.0 / D ** 0.5, mask == "causal", nthreads=threads, lib=lib)
+    return time.perf_counter() - t0, out
+
+
+def cpu_baseline() -> dict:
+    """The oracle on two whole heads of the workload (one per mask)."""
+    import oracle
+    from deterministic_attn_backward_gb300 import inputs
+    q, k, v, do = inputs.make_qkvdo(B, H, S, D, SEED, QK_SCALE)
+    lib, threads = oracle.load(), oracle.default_threads()
+    secs = fl = 0.0
+    for (b, h), m in (((0, 0), "causal"), ((B - 1, H - 1), "full")):
+        dt, _ = _oracle_head_time(q, k, v, do, b, h, m, lib, threads)
+        secs += dt
+        fl += flops(m) / (B * H)
+    return {"value": round(fl / secs / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"2 whole heads of the workload (head (0,0) causal, head ({B-1},{H-1}) full),"
+                      f" float64 forward+backward, {secs:.1f} s"}
+
+
+def run_reference(args, rank: int) -> dict | None:
+    """The oracle as it stands, on bounded row samples of the workload.
+
+    Set-up (untimed): one whole head per mask through the oracle, for the
+    LSE_r and D_r every key row needs.  Each step then recomputes, for that
+    head, ROWS query rows (O, LSE, D, dQ) and ROWS key rows (dK, dV) per mask,
+    rotating the rows from step to step; one query row plus one key row is
+    1/S of the head's backward FLOPs.
+    """
+    if rank != 0:
+        return None
+    import oracle
+    from deterministic_attn_backward_gb300 import inputs
+    rows_per_step = 64
+    q, k, v, do = inputs.make_qkvdo(B, H, S, D, SEED, QK_SCALE)
+    lib, threads = oracle.load(), oracle.default_threads()
+    prep = {}
+    for (b, h), m in (((0, 0), "causal"), ((B - 1, H - 1), "full")):
+        _, whole = _oracle_head_time(q, k, v, do, b, h, m, lib, threads)
+        prep[m] = ([t[b, h] for t in (q, k, v, do)], whole["lse"][0], whole["D"][0])
+    secs = fl = 0.0
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        f = 0.0
+        for m in MASKS:
+            args_h, lse_all, D_all = prep[m]
+            rows = [((i * rows_per_step + x) * 97) % S for x in range(rows_per_step)]
+            oracle.attn_rows(*args_h, 1.0 / D ** 0.5, m == "causal", rows, rows,
+                             lse_all=lse_all, D_all=D_all, nthreads=threads, lib=lib)
+            f += flops(m) / (B * H) * (2 * rows_per_step) / (2 * S)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            secs += dt
+            fl += f
+    value = fl / secs / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / max(1, args.steps) * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(), "B": B, "H": H, "S": S, "d": D,
+                   "masks": list(MASKS), "seed": SEED, "qk_scale": QK_SCALE},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"per step and mask: {rows_per_step} query rows (O, LSE, D, dQ)"
+                                   f" and {rows_per_step} key rows (dK, dV) of one head, float64;"
+                                   " the head's LSE and D computed once, untimed"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        out = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()
