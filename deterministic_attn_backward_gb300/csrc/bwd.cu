@@ -23,8 +23,9 @@
 //   warp 0      TMA producer (K_i, V_i per chain; Q_j, dO_j, LSE_j, D_j per
 //               step, double-buffered) and tensor-memory allocation
 //   warp 1      MMA issuer (one thread)
-//   warps 4-7   softmax / dS warpgroup (thread = KV row), chain epilogue
-//   warps 8-15  dQ reducers (two warpgroups, one half of the tile each)
+//   warps 4-11  softmax / dS, two warpgroups of 64 Q columns each (thread =
+//               KV row), and the chain epilogue (dV by one, dK by the other)
+//   warps 12-15 dQ reducer
 // Every wait is bounded: on expiry the kernel records DAB_ERR_TIMEOUT in the
 // workspace and every role drains and returns.
 #include <cuda.h>
@@ -39,9 +40,9 @@ namespace dab {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kSoftmaxWarp0 = 4;
-constexpr int kReducerWarp0 = 8;
-constexpr int kNumReducerThreads = 256;
+constexpr int kSoftmaxWarp0 = 4;    // warps 4-7: columns 0-63, warps 8-11: columns 64-127
+constexpr int kReducerWarp0 = 12;   // warps 12-15
+constexpr int kNumReducerThreads = 128;
 constexpr uint32_t kReducerBar = 1;  // named barrier id
 
 template <int HD>
@@ -90,8 +91,7 @@ struct Misc {
   // the whole group after a named barrier (so the group always takes the same
   // path through its barriers).
   int red_unit;
-  int red_dq_ok[2];
-  int red_sem_ok[2];
+  int red_ok[2];
 };
 static_assert(sizeof(Misc) <= 64, "misc block");
 
@@ -140,20 +140,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     mbar_init(&bars->kv_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->q_full[s], 1);
-      mbar_init(&bars->q_empty[s], 1 + 4);
+      mbar_init(&bars->q_empty[s], 1 + 8);
       mbar_init(&bars->unit_full[s], 1);
-      mbar_init(&bars->unit_empty[s], 1 + 4 + 8);
+      mbar_init(&bars->unit_empty[s], 1 + 8 + 4);
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_full, 4);
-    mbar_init(&bars->ds_full, 4);
+    mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->ds_full, 8);
     mbar_init(&bars->dv_done, 1);
     mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_empty, 8);
+    mbar_init(&bars->dq_empty, 4);
     mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, 4);
+    mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
     misc->abort = 0;
     fence_mbar_init();
@@ -235,10 +235,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per step s (tile i, j): dV(s), dQ(s), then S(s+1) of the next step of
+    // the same chain, dK(s), dP(s+1).  S(s+1) and dP(s+1) thus run while the
+    // softmax warps still work on step s, dK(s) hides the reducer's drain of
+    // dQ(s), and the tensor pipe always has work queued.  At a chain boundary
+    // S and dP of the new chain's first step are issued once its K/V landed.
     if (lane == 0) {
       const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sDS = sbase + C::kOffDS;
+      auto issue_s = [&](int stage) {
+        const uint32_t sQ = sbase + C::kOffQ + stage * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(tbase + C::kColS, desc_kmajor(sK, k, 128), desc_kmajor(sQ, k, 128), C::kIdS, k > 0);
+        mma_commit(&bars->s_full);
+      };
+      auto issue_dp = [&](int stage) {
+        const uint32_t sDO = sbase + C::kOffDO + stage * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(tbase + C::kColDP, desc_kmajor(sV, k, 128), desc_kmajor(sDO, k, 128), C::kIdS, k > 0);
+        mma_commit(&bars->dp_full);
+      };
       int s = 0, chain = 0, uidx = 0;
-      bool ok = true;
+      bool ok = true, pre = false;
       while (ok) {
         const int slot = uidx & 1;
         if (!mbar_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 10)) break;
@@ -253,55 +272,63 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           const int stage = s & 1;
           const uint32_t sQ = sbase + C::kOffQ + stage * C::kTileBytes;
           const uint32_t sDO = sbase + C::kOffDO + stage * C::kTileBytes;
-          if (st.chain_first && !mbar_wait(&bars->kv_full, chain & 1, wc, 11)) { ok = false; break; }
-          if (!mbar_wait(&bars->q_full[stage], (s >> 1) & 1, wc, 12)) { ok = false; break; }
-          // S^T = K Q^T (the previous P^T must have been consumed by its dV MMA)
-          if (s > 0 && !mbar_wait(&bars->dv_done, (s - 1) & 1, wc, 13)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < HD / 16; ++k)
-            mma_ss(tbase + C::kColS, desc_kmajor(sK, k, 128), desc_kmajor(sQ, k, 128), C::kIdS, k > 0);
-          mma_commit(&bars->s_full);
-          // dP^T = V dO^T (for d = 128 it lands where the previous dQ^T was)
-          if (HD == 128 && s > 0 && !mbar_wait(&bars->dq_empty, (s - 1) & 1, wc, 14)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < HD / 16; ++k)
-            mma_ss(tbase + C::kColDP, desc_kmajor(sV, k, 128), desc_kmajor(sDO, k, 128), C::kIdS, k > 0);
-          mma_commit(&bars->dp_full);
-          // dV += P^T dO, P^T from tensor memory
+          if (!pre) {
+            if (st.chain_first && !mbar_wait(&bars->kv_full, chain & 1, wc, 11)) { ok = false; break; }
+            if (!mbar_wait(&bars->q_full[stage], (s >> 1) & 1, wc, 12)) { ok = false; break; }
+            if (s > 0 && !mbar_wait(&bars->dv_done, (s - 1) & 1, wc, 13)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(stage);
+            if (HD == 128 && s > 0 && !mbar_wait(&bars->dq_empty, (s - 1) & 1, wc, 14)) { ok = false; break; }
+            tc_fence_after();
+            issue_dp(stage);
+          }
+          // dV += P^T dO; P^T from tensor memory, its two 64-column halves
+          // packed at the start of each half of the S columns
           if (!mbar_wait(&bars->p_full, s & 1, wc, 15)) { ok = false; break; }
           if (st.chain_first && chain > 0 && !mbar_wait(&bars->acc_empty, (chain - 1) & 1, wc, 16)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_ts(tbase + C::kColDV, tbase + C::kColS + 8 * k, desc_mnmajor(sDO, k, 128), C::kIdAcc,
-                   !(st.chain_first && k == 0));
+            mma_ts(tbase + C::kColDV, tbase + C::kColS + (k >> 2) * 64 + (k & 3) * 8,
+                   desc_mnmajor(sDO, k, 128), C::kIdAcc, !(st.chain_first && k == 0));
           mma_commit(&bars->dv_done);
-          // dK += dS^T Q ; dQ partial
+          // dQ partial (d = 128: dQ^T = K^T dS^T; d = 64: dQ = dS K)
           if (!mbar_wait(&bars->ds_full, s & 1, wc, 17)) { ok = false; break; }
           if (HD == 64 && s > 0 && !mbar_wait(&bars->dq_empty, (s - 1) & 1, wc, 18)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)
-            mma_ss(tbase + C::kColDK, desc_kmajor(sDS, k, 128), desc_mnmajor(sQ, k, 128), C::kIdAcc,
-                   !(st.chain_first && k == 0));
-          mma_commit(&bars->q_empty[stage]);
-#pragma unroll
           for (int k = 0; k < kTile / 16; ++k) {
-            // d = 128: dQ^T = K^T dS^T (A = K, MN-major; B = dS^T, MN-major)
-            // d =  64: dQ   = dS K     (A = dS, MN-major; B = K, MN-major)
             const uint64_t a = (HD == 128) ? desc_mnmajor(sK, k, 128) : desc_mnmajor(sDS, k, 128);
             const uint64_t b = (HD == 128) ? desc_mnmajor(sDS, k, 128) : desc_mnmajor(sK, k, 128);
             mma_ss(tbase + C::kColDQ, a, b, C::kIdDQ, k > 0);
           }
           mma_commit(&bars->dq_full);
+          const bool next = !st.chain_last;  // the next step continues this chain
+          if (next) {
+            const int st1 = (s + 1) & 1;
+            if (!mbar_wait(&bars->q_full[st1], ((s + 1) >> 1) & 1, wc, 19)) { ok = false; break; }
+            if (!mbar_wait(&bars->dv_done, s & 1, wc, 20)) { ok = false; break; }  // P^T(s) consumed
+            tc_fence_after();
+            issue_s(st1);
+          }
+          // dK += dS^T Q
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_ss(tbase + C::kColDK, desc_kmajor(sDS, k, 128), desc_mnmajor(sQ, k, 128), C::kIdAcc,
+                   !(st.chain_first && k == 0));
+          mma_commit(&bars->q_empty[stage]);
           mma_commit(&bars->ds_free);
           if (st.chain_last) {
             mma_commit(&bars->acc_full);
             mma_commit(&bars->kv_empty);
             ++chain;
           }
+          if (next) {
+            if (HD == 128 && !mbar_wait(&bars->dq_empty, s & 1, wc, 21)) { ok = false; break; }
+            tc_fence_after();
+            issue_dp((s + 1) & 1);
+          }
+          pre = next;
           ++s;
         }
       }
@@ -312,15 +339,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     __syncwarp();
   } else if (warp >= kSoftmaxWarp0 && warp < kReducerWarp0) {
     // ------------------------------------------------------ softmax / dS
+    // Two warpgroups; warpgroup h owns Q columns 64h .. 64h+63 of the tile.
+    const int h = (warp - kSoftmaxWarp0) >> 2;
     const int quad = warp & 3;                 // tensor-memory lane quadrant
     const int r = quad * 32 + lane;            // KV row of the tile
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    uint8_t* sds = smem + C::kOffDS;
+    uint8_t* sds = smem + C::kOffDS + h * 16384;
     int s = 0, chain = 0, uidx = 0;
     bool ok = true;
     while (ok) {
       const int slot = uidx & 1;
-      if (!warp_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 20)) break;
+      if (!warp_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 30)) break;
       const int U = misc->ring[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->unit_empty[slot]);
@@ -331,44 +360,46 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       for (int t = 0; t < steps; ++t) {
         const Step st = step(p.sched, p.mask, p.N, u, t);
         const int stage = s & 1;
-        const float* lse = s_lse + stage * 128;
-        const float* dd = s_dd + stage * 128;
+        const float* lse = s_lse + stage * 128 + 64 * h;
+        const float* dd = s_dd + stage * 128 + 64 * h;
         const bool diag = (p.mask == kMaskCausal) && (st.kv == st.q);
-        if (!warp_wait(&bars->q_full[stage], (s >> 1) & 1, wc, 21)) { ok = false; break; }
-        if (!warp_wait(&bars->s_full, s & 1, wc, 22)) { ok = false; break; }
+        if (!warp_wait(&bars->q_full[stage], (s >> 1) & 1, wc, 31)) { ok = false; break; }
+        if (!warp_wait(&bars->s_full, s & 1, wc, 32)) { ok = false; break; }
         tc_fence_after();
-        // P^T = exp2(S^T * scale*log2(e) - LSE*log2(e)), packed to bf16 in place.
-        uint32_t pk[64];
+        // P^T = exp2(S^T * scale*log2(e) - LSE*log2(e)), bf16 pairs written
+        // over the columns this warpgroup has just read.
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32(tbase + lane_off + C::kColS + 32 * c, v);
+          tmem_ld32(tbase + lane_off + C::kColS + 64 * h + 32 * c, v);
           uint32_t w16[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const int col = 32 * c + e;
+            const int col = 32 * c + e;          // column within this half
             float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2e, -lse[col]));
             float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2e, -lse[col + 1]));
             if (diag) {
-              if (r > col) p0 = 0.f;
-              if (r > col + 1) p1 = 0.f;
+              const int qc = 64 * h + col;       // Q column within the tile
+              if (r > qc) p0 = 0.f;
+              if (r > qc + 1) p1 = 0.f;
             }
             w16[e >> 1] = pack_bf16x2(p0, p1);
             pk[16 * c + (e >> 1)] = w16[e >> 1];
           }
-          tmem_st16(tbase + lane_off + C::kColS + 16 * c, w16);
+          tmem_st16(tbase + lane_off + C::kColS + 64 * h + 16 * c, w16);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full);
-        // dS^T = P^T o (dP^T - D) -> shared memory (bf16, 128B-swizzled)
-        if (!warp_wait(&bars->dp_full, s & 1, wc, 23)) { ok = false; break; }
-        if (s > 0 && !warp_wait(&bars->ds_free, (s - 1) & 1, wc, 24)) { ok = false; break; }
+        // dS^T = P^T o (dP^T - D) -> shared memory block h (bf16, 128B-swizzled)
+        if (!warp_wait(&bars->dp_full, s & 1, wc, 33)) { ok = false; break; }
+        if (s > 0 && !warp_wait(&bars->ds_free, (s - 1) & 1, wc, 34)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32(tbase + lane_off + C::kColDP + 32 * c, v);
+          tmem_ld32(tbase + lane_off + C::kColDP + 64 * h + 32 * c, v);
           uint32_t w16[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -380,12 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             const float ds1 = p1 * (__uint_as_float(v[e + 1]) - dd[col + 1]);
             w16[e >> 1] = pack_bf16x2(ds0, ds1);
           }
-          uint8_t* rowp = sds + (c >> 1) * 16384 + r * 128;
+          uint8_t* rowp = sds + r * 128;
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
-            const int cc = (c & 1) * 4 + m;
-            uint4 val = make_uint4(w16[4 * m], w16[4 * m + 1], w16[4 * m + 2], w16[4 * m + 3]);
-            *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = val;
+            const int cc = c * 4 + m;
+            *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) =
+                make_uint4(w16[4 * m], w16[4 * m + 1], w16[4 * m + 2], w16[4 * m + 3]);
           }
         }
         fence_proxy_async_smem();
@@ -396,27 +427,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           mbar_arrive(&bars->q_empty[stage]);
         }
         if (st.chain_last) {
-          // Epilogue: dV_i = bf16(dV acc), dK_i = bf16(scale * dK acc).
-          if (!warp_wait(&bars->acc_full, chain & 1, wc, 25)) { ok = false; break; }
+          // Epilogue: warpgroup 0 writes dV_i = bf16(dV acc), warpgroup 1
+          // writes dK_i = bf16(scale * dK acc).
+          if (!warp_wait(&bars->acc_full, chain & 1, wc, 35)) { ok = false; break; }
           tc_fence_after();
           const size_t row = (size_t)bh * p.S + (size_t)st.kv * kTile + r;
+          __nv_bfloat16* out = (h == 0 ? p.dv : p.dk) + row * HD;
+          const uint32_t col0 = (h == 0) ? C::kColDV : C::kColDK;
+          const float sc = (h == 0) ? 1.0f : p.scale;
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t v[32];
-            tmem_ld32(tbase + lane_off + C::kColDV + 32 * c, v);
-            uint4* dst = reinterpret_cast<uint4*>(p.dv + row * HD + 32 * c);
+            tmem_ld32(tbase + lane_off + col0 + 32 * c, v);
+            uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
 #pragma unroll
             for (int m = 0; m < 4; ++m)
-              dst[m] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * m]), __uint_as_float(v[8 * m + 1])),
-                                  pack_bf16x2(__uint_as_float(v[8 * m + 2]), __uint_as_float(v[8 * m + 3])),
-                                  pack_bf16x2(__uint_as_float(v[8 * m + 4]), __uint_as_float(v[8 * m + 5])),
-                                  pack_bf16x2(__uint_as_float(v[8 * m + 6]), __uint_as_float(v[8 * m + 7])));
-            tmem_ld32(tbase + lane_off + C::kColDK + 32 * c, v);
-            uint4* dstk = reinterpret_cast<uint4*>(p.dk + row * HD + 32 * c);
-            const float sc = p.scale;
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-              dstk[m] = make_uint4(
+              dst[m] = make_uint4(
                   pack_bf16x2(sc * __uint_as_float(v[8 * m]), sc * __uint_as_float(v[8 * m + 1])),
                   pack_bf16x2(sc * __uint_as_float(v[8 * m + 2]), sc * __uint_as_float(v[8 * m + 3])),
                   pack_bf16x2(sc * __uint_as_float(v[8 * m + 4]), sc * __uint_as_float(v[8 * m + 5])),
@@ -431,12 +457,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       }
     }
   } else if (warp >= kReducerWarp0) {
-    // ------------------------------------------------------ dQ reducers
-    // The leader (first reducer thread) does every wait; the group follows
-    // its decisions through shared-memory slots read after a named barrier,
-    // so all 256 threads always pass the same barriers.
+    // ------------------------------------------------------ dQ reducer
+    // One warpgroup.  The leader (first reducer thread) does every wait; the
+    // group follows its decisions through shared-memory slots read after a
+    // named barrier, so all 128 threads always pass the same barriers.  For
+    // the ordered schedules the leader waits for its turn on the semaphore
+    // while the tensor cores still compute the partial.
     const int quad = warp & 3;
-    const int half = (warp - kReducerWarp0) >> 2;
     const int r = quad * 32 + lane;  // tensor-memory lane: d index (d=128) or Q row (d=64)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const bool leader = (threadIdx.x == kReducerWarp0 * 32);
@@ -446,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     while (ok) {
       const int slot = uidx & 1;
       if (leader) {
-        vm->red_unit = mbar_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 30) ? vm->ring[slot] : -2;
+        vm->red_unit = mbar_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 40) ? vm->ring[slot] : -2;
       }
       named_bar_sync(kReducerBar, kNumReducerThreads);
       const int U = vm->red_unit;
@@ -457,62 +484,61 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       const int steps = unit_steps(p.sched, p.mask, p.N, u);
       for (int t = 0; t < steps; ++t) {
         const Step st = step(p.sched, p.mask, p.N, u, t);
-        if (leader) vm->red_dq_ok[s & 1] = mbar_wait(&bars->dq_full, s & 1, wc, 31) ? 1 : 0;
+        const int rank = deterministic ? dab::rank(p.sched, p.mask, p.N, st.kv, st.q) : 0;
+        uint32_t* sem = p.sem + (size_t)bh * p.N + st.q;
+        if (leader) {
+          bool g = true;
+          if (deterministic)
+            g = sem_wait(sem, (uint32_t)rank, wc, (uint32_t)(bh * p.N + st.q));
+          if (g) g = mbar_wait(&bars->dq_full, s & 1, wc, 41);
+          vm->red_ok[s & 1] = g ? 1 : 0;
+        }
         named_bar_sync(kReducerBar, kNumReducerThreads);
-        if (!vm->red_dq_ok[s & 1]) { ok = false; break; }
+        if (!vm->red_ok[s & 1]) { ok = false; break; }
         tc_fence_after();
-        constexpr int kVals = (HD == 128) ? 64 : 32;
-        float val[kVals];
-        {
-          uint32_t v[32];
+        const bool store = deterministic && rank == 0;  // the first contribution overwrites
+        const size_t row0 = (size_t)bh * p.S + (size_t)st.q * kTile;
+        if (HD == 128) {
+          // thread = d index r; 32-column chunks = Q rows 32c .. 32c+31
+          float* base = p.dqacc + row0 * HD + r;
 #pragma unroll
-          for (int c = 0; c < kVals / 32; ++c) {
-            tmem_ld32(tbase + lane_off + C::kColDQ + (uint32_t)(half * kVals + 32 * c), v);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + lane_off + C::kColDQ + 32 * c, v);
+            float* b2 = base + (size_t)(32 * c) * HD;
+            if (store) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) val[32 * c + e] = __uint_as_float(v[e]);
+              for (int e = 0; e < 32; ++e) b2[(size_t)e * HD] = __uint_as_float(v[e]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) red_add_f32(b2 + (size_t)e * HD, __uint_as_float(v[e]));
+            }
+          }
+        } else {
+          // thread = Q row r; 32-column chunks = d columns 32c .. 32c+31
+          float* base = p.dqacc + (row0 + (size_t)r) * HD;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + lane_off + C::kColDQ + 32 * c, v);
+            float* b2 = base + 32 * c;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              const float a0 = __uint_as_float(v[4 * m]), a1 = __uint_as_float(v[4 * m + 1]);
+              const float a2 = __uint_as_float(v[4 * m + 2]), a3 = __uint_as_float(v[4 * m + 3]);
+              if (store)
+                reinterpret_cast<float4*>(b2)[m] = make_float4(a0, a1, a2, a3);
+              else
+                red_add_v4_f32(b2 + 4 * m, a0, a1, a2, a3);
+            }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->dq_empty);
-        int rank = 0;
-        uint32_t* sem = p.sem + (size_t)bh * p.N + st.q;
         if (deterministic) {
-          rank = dab::rank(p.sched, p.mask, p.N, st.kv, st.q);
-          if (leader)
-            vm->red_sem_ok[s & 1] = sem_wait(sem, (uint32_t)rank, wc, (uint32_t)(bh * p.N + st.q)) ? 1 : 0;
-          named_bar_sync(kReducerBar, kNumReducerThreads);
-          if (!vm->red_sem_ok[s & 1]) { ok = false; break; }
-        }
-        const size_t row0 = (size_t)bh * p.S + (size_t)st.q * kTile;
-        if (HD == 128) {
-          // thread = d index; values = Q rows half*64 .. half*64+63
-          float* base = p.dqacc + (row0 + (size_t)half * 64) * HD + r;
-          if (deterministic && rank == 0) {
-#pragma unroll
-            for (int q = 0; q < 64; ++q) base[(size_t)q * HD] = val[q];
-          } else {
-#pragma unroll
-            for (int q = 0; q < 64; ++q) red_add_f32(base + (size_t)q * HD, val[q]);
-          }
-        } else {
-          // thread = Q row; values = d columns half*32 .. half*32+31
-          float* base = p.dqacc + (row0 + (size_t)r) * HD + half * 32;
-          if (deterministic && rank == 0) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m)
-              reinterpret_cast<float4*>(base)[m] =
-                  make_float4(val[4 * m], val[4 * m + 1], val[4 * m + 2], val[4 * m + 3]);
-          } else {
-#pragma unroll
-            for (int m = 0; m < 8; ++m)
-              red_add_v4_f32(base + 4 * m, val[4 * m], val[4 * m + 1], val[4 * m + 2], val[4 * m + 3]);
-          }
-        }
-        if (deterministic) {
-          // Publish: every reducer's adds are ordered before the release of
-          // rank + 1 (fence per thread, then the barrier, then the leader's
-          // release store).
+          // Publish: every reducer thread's writes are ordered before the
+          // release of rank + 1 (fence per thread, barrier, leader's release).
           fence_acq_rel_gpu();
           named_bar_sync(kReducerBar, kNumReducerThreads);
           if (leader) st_release_gpu(sem, (uint32_t)rank + 1u);

@@ -34,8 +34,13 @@ def test_bitwise_repeatable(mask, sched, d):
 @pytest.mark.gpu
 @pytest.mark.parametrize("mask", ["full", "causal"])
 @pytest.mark.parametrize("d", [64, 128])
-def test_descending_equals_serial_bitwise(mask, d):
+def test_descending_keeps_serial_dq_bits(mask, d):
+    """Descending Q-tile iteration keeps the serial schedule's dQ reduction
+    order, so dQ is bitwise equal.  dK and dV accumulate on chip along the
+    chain, whose Q-tile order descending reverses: equal within tolerance."""
     a = _grads(2, 4, 1024, d, mask, "serial", 1)[0]
     b = _grads(2, 4, 1024, d, mask, "descending_q", 1)[0]
-    for x, y in zip(a, b):
-        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    for x, y in zip(a[1:], b[1:]):
+        err = (x.double() - y.double()).abs().max() / y.double().abs().max()
+        assert err < 1e-2
