@@ -371,13 +371,48 @@ def run_reference(args, rank: int) -> dict | None:
     }
 
 
+def run_case(spec: str, reps: int) -> dict:
+    """One configuration "B,H,S,d,mask,sched": `reps` backward calls after
+    three warm-up calls, each timed with CUDA events (used to drive profilers
+    and size sweeps; prints per-call milliseconds and TFLOP/s)."""
+    import torch
+    import deterministic_attn_backward_gb300 as dab
+    from deterministic_attn_backward_gb300 import inputs
+    b, h, s_, d = (int(x) for x in spec.split(",")[:4])
+    mask, sched = spec.split(",")[4:6]
+    q, k, v, do = (t.cuda() for t in inputs.make_qkvdo(b, h, s_, d, 7, 0.5))
+    o, lse = dab.attn_fwd(q, k, v, mask)
+    ws = dab.new_workspace(b, h, s_, d, mask, sched)
+    out = tuple(torch.empty_like(q) for _ in range(3))
+    ms = []
+    for i in range(3 + reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dab.attn_bwd(q, k, v, o, lse, do, mask, sched, workspace=ws, out=out)
+        e1.record()
+        e1.synchronize()
+        if i >= 3:
+            ms.append(e0.elapsed_time(e1))
+    st = dab.check_status(ws)
+    f = 10.0 * b * h * s_ * s_ * d * (1.0 if mask == "full" else 0.5)
+    med = statistics.median(ms)
+    return {"case": spec, "status": st, "ms": [round(x, 4) for x in ms],
+            "tflops": round(f / med / 1e9, 2)}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--case", default=None, help="B,H,S,d,mask,sched: time one configuration")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.case:
+        for spec in args.case.split(";"):
+            print(json.dumps(run_case(spec, args.reps)), flush=True)
+        return
     args.warmup = max(3, args.warmup)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

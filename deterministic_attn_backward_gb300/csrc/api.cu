@@ -132,7 +132,7 @@ bool layout(int B, int H, int S, int d, dab_ws_layout_t* L) {
   L->status = off;
   off += 256;
   L->sem = off;
-  off = round_up(off + BH * N * 4, 256);
+  off = round_up(off + BH * N * 4 * 4, 256);  // 4 semaphores per dQ tile
   L->D = off;
   off = round_up(off + rows * 4, 256);
   L->lse2 = off;
@@ -227,7 +227,7 @@ dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dou
   if (!device_setup(nullptr, &sms)) return DAB_ERR_UNSUPPORTED;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const long long rows = (long long)B * H * S;
-  const int n_sem = B * H * (S / 128);
+  const int n_sem = B * H * (S / 128) * 4;
   float* dqacc = (sched == DAB_SCHED_ATOMIC) ? reinterpret_cast<float*>(ws + L.dqacc) : nullptr;
   const int grid = elementwise_grid(sms, rows * (d / 8));
   cudaError_t e = dab::launch_preprocess(
@@ -300,7 +300,7 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(512);
+  cfg.blockDim = dim3(448);
   cfg.dynamicSmemBytes = (d == 128) ? dab::bwd_smem_bytes<128>() : dab::bwd_smem_bytes<64>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

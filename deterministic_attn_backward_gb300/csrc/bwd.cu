@@ -16,16 +16,16 @@
 // written once at its end.  The dQ partial is added to an f32 accumulator in
 // global memory by the reducer warps: for the deterministic schedules in the
 // fixed order rank(i, j) (technical summary section 1: a fixed accumulation
-// order for dQ), waiting on a per-(head, Q tile) semaphore with acquire loads
+// order for dQ), waiting on per-(head, Q tile, quarter) semaphores with acquire loads
 // and publishing with a release store; for ATOMIC with unordered float adds.
 //
-// Warp roles (16 warps):
+// Warp roles (14 warps):
 //   warp 0      TMA producer (K_i, V_i per chain; Q_j, dO_j, LSE_j, D_j per
 //               step, double-buffered) and tensor-memory allocation
 //   warp 1      MMA issuer (one thread)
-//   warps 4-11  softmax / dS, two warpgroups of 64 Q columns each (thread =
-//               KV row), and the chain epilogue (dV by one, dK by the other)
-//   warps 12-15 dQ reducer
+//   warps 2-9   softmax / dS, two groups of four warps, 64 Q columns each
+//               (thread = KV row), and the chain epilogue (dV / dK)
+//   warps 10-13 dQ reducer, one quarter of the dQ tile and one semaphore each
 // Every wait is bounded: on expiry the kernel records DAB_ERR_TIMEOUT in the
 // workspace and every role drains and returns.
 #include <cuda.h>
@@ -39,11 +39,10 @@
 namespace dab {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kSoftmaxWarp0 = 4;    // warps 4-7: columns 0-63, warps 8-11: columns 64-127
-constexpr int kReducerWarp0 = 12;   // warps 12-15
-constexpr int kNumReducerThreads = 128;
-constexpr uint32_t kReducerBar = 1;  // named barrier id
+constexpr int kThreads = 448;       // 14 warps (launch configuration; 144 registers each)
+constexpr int kSoftmaxWarp0 = 2;    // warps 2-5: columns 0-63, warps 6-9: columns 64-127
+constexpr int kReducerWarp0 = 10;   // warps 10-13
+constexpr int kSubTiles = 4;        // dQ tile = 4 sub-tiles, one semaphore and reducer warp each
 
 template <int HD>
 struct Cfg {
@@ -87,11 +86,6 @@ struct Misc {
   uint32_t tmem_base;
   int abort;
   int ring[2];
-  // Reducer-group control slots, written by the reducer leader and read by
-  // the whole group after a named barrier (so the group always takes the same
-  // path through its barriers).
-  int red_unit;
-  int red_ok[2];
 };
 static_assert(sizeof(Misc) <= 64, "misc block");
 
@@ -118,7 +112,7 @@ static __device__ __noinline__ bool sem_wait(const uint32_t* sem, uint32_t targe
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __maxnreg__(144) bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = Cfg<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
@@ -458,90 +452,80 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp >= kReducerWarp0) {
     // ------------------------------------------------------ dQ reducer
-    // One warpgroup.  The leader (first reducer thread) does every wait; the
-    // group follows its decisions through shared-memory slots read after a
-    // named barrier, so all 128 threads always pass the same barriers.  For
-    // the ordered schedules the leader waits for its turn on the semaphore
-    // while the tensor cores still compute the partial.
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // tensor-memory lane: d index (d=128) or Q row (d=64)
+    // Four warps.  Each drains its tensor-memory quadrant of the dQ partial
+    // into registers at once (so the tensor memory is free for the next
+    // partial), then adds its fixed quarter of the tile into the f32
+    // accumulator: d columns 32w..32w+31 of all 128 Q rows for d = 128
+    // (dQ^T: lanes = d), Q rows 32w..32w+31 for d = 64 (dQ: lanes = Q rows).
+    // For the ordered schedules every quarter has its own semaphore, so
+    // consecutive contributors to one dQ tile overlap on different quarters
+    // while each element still receives its partial sums in rank order.
+    const int quad = warp & 3;       // tensor-memory lane quadrant = sub-tile
+    const int r = quad * 32 + lane;  // d index (d = 128) or Q row (d = 64)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const bool leader = (threadIdx.x == kReducerWarp0 * 32);
-    volatile Misc* vm = misc;
     int s = 0, uidx = 0;
     bool ok = true;
     while (ok) {
       const int slot = uidx & 1;
-      if (leader) {
-        vm->red_unit = mbar_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 40) ? vm->ring[slot] : -2;
-      }
-      named_bar_sync(kReducerBar, kNumReducerThreads);
-      const int U = vm->red_unit;
-      if (lane == 0 && U != -2) mbar_arrive(&bars->unit_empty[slot]);
+      if (!warp_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 40)) break;
+      const int U = misc->ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->unit_empty[slot]);
       ++uidx;
       if (U < 0) break;
       const int bh = U / p.units_per_head, u = U % p.units_per_head;
       const int steps = unit_steps(p.sched, p.mask, p.N, u);
       for (int t = 0; t < steps; ++t) {
         const Step st = step(p.sched, p.mask, p.N, u, t);
+        // everything but the values is computed before the drain
         const int rank = deterministic ? dab::rank(p.sched, p.mask, p.N, st.kv, st.q) : 0;
-        uint32_t* sem = p.sem + (size_t)bh * p.N + st.q;
-        if (leader) {
-          bool g = true;
-          if (deterministic)
-            g = sem_wait(sem, (uint32_t)rank, wc, (uint32_t)(bh * p.N + st.q));
-          if (g) g = mbar_wait(&bars->dq_full, s & 1, wc, 41);
-          vm->red_ok[s & 1] = g ? 1 : 0;
-        }
-        named_bar_sync(kReducerBar, kNumReducerThreads);
-        if (!vm->red_ok[s & 1]) { ok = false; break; }
-        tc_fence_after();
+        uint32_t* sem = p.sem + ((size_t)bh * p.N + st.q) * kSubTiles + quad;
+        const uint32_t sem_detail = (uint32_t)((bh * p.N + st.q) * kSubTiles + quad);
         const bool store = deterministic && rank == 0;  // the first contribution overwrites
         const size_t row0 = (size_t)bh * p.S + (size_t)st.q * kTile;
-        if (HD == 128) {
-          // thread = d index r; 32-column chunks = Q rows 32c .. 32c+31
-          float* base = p.dqacc + row0 * HD + r;
+        float* base = (HD == 128) ? p.dqacc + row0 * HD + r        // column r of Q rows 0..127
+                                  : p.dqacc + (row0 + (size_t)r) * HD;  // Q row r, d 0..63
+        if (!warp_wait(&bars->dq_full, s & 1, wc, 41)) { ok = false; break; }
+        tc_fence_after();
+        constexpr int kVals = (HD == 128) ? 128 : 64;
+        uint32_t v[kVals];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tbase + lane_off + C::kColDQ + 32 * c, v);
-            float* b2 = base + (size_t)(32 * c) * HD;
-            if (store) {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) b2[(size_t)e * HD] = __uint_as_float(v[e]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) red_add_f32(b2 + (size_t)e * HD, __uint_as_float(v[e]));
-            }
-          }
-        } else {
-          // thread = Q row r; 32-column chunks = d columns 32c .. 32c+31
-          float* base = p.dqacc + (row0 + (size_t)r) * HD;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tbase + lane_off + C::kColDQ + 32 * c, v);
-            float* b2 = base + 32 * c;
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-              const float a0 = __uint_as_float(v[4 * m]), a1 = __uint_as_float(v[4 * m + 1]);
-              const float a2 = __uint_as_float(v[4 * m + 2]), a3 = __uint_as_float(v[4 * m + 3]);
-              if (store)
-                reinterpret_cast<float4*>(b2)[m] = make_float4(a0, a1, a2, a3);
-              else
-                red_add_v4_f32(b2 + 4 * m, a0, a1, a2, a3);
-            }
-          }
-        }
+        for (int c = 0; c < kVals / 32; ++c)
+          tmem_ld32(tbase + lane_off + C::kColDQ + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->dq_empty);
         if (deterministic) {
-          // Publish: every reducer thread's writes are ordered before the
-          // release of rank + 1 (fence per thread, barrier, leader's release).
+          int g = 1;
+          if (lane == 0) g = sem_wait(sem, (uint32_t)rank, wc, sem_detail) ? 1 : 0;
+          g = __shfl_sync(0xffffffffu, g, 0);
+          if (!g) { ok = false; break; }
+        }
+        if (HD == 128) {
+          if (store) {
+#pragma unroll
+            for (int q = 0; q < 128; ++q) base[(size_t)q * HD] = __uint_as_float(v[q]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 128; ++q) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
+          }
+        } else {
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            const float a0 = __uint_as_float(v[4 * m]), a1 = __uint_as_float(v[4 * m + 1]);
+            const float a2 = __uint_as_float(v[4 * m + 2]), a3 = __uint_as_float(v[4 * m + 3]);
+            if (store)
+              reinterpret_cast<float4*>(base)[m] = make_float4(a0, a1, a2, a3);
+            else
+              red_add_v4_f32(base + 4 * m, a0, a1, a2, a3);
+          }
+        }
+        if (deterministic) {
+          // Publish: the warp's writes are ordered before the release of
+          // rank + 1 (fence per lane, warp barrier, lane 0's release store).
           fence_acq_rel_gpu();
-          named_bar_sync(kReducerBar, kNumReducerThreads);
-          if (leader) st_release_gpu(sem, (uint32_t)rank + 1u);
+          __syncwarp();
+          if (lane == 0) st_release_gpu(sem, (uint32_t)rank + 1u);
         }
         ++s;
       }

@@ -95,7 +95,8 @@ dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v,
 
 /* Bytes of device workspace that dab_attn_bwd needs for this problem (0 on
  * invalid arguments).  The workspace holds the status word, the dispatch
- * counter, one semaphore per 128-row dQ tile, D and LSE*log2(e) per row, and
+ * counter, four semaphores per 128-row dQ tile (one per quarter), D and
+ * LSE*log2(e) per row, and
  * the float32 dQ accumulator [B][H][S][d].  It needs no initialisation: the
  * first kernel of every backward call resets what must start at zero.      */
 size_t dab_bwd_workspace_size(int B, int H, int S, int d,
@@ -164,7 +165,7 @@ dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dou
 /* Byte offsets of the workspace regions (for tests and tools).             */
 typedef struct {
     size_t status;   /* uint32 status word, uint32 error detail, uint32 counter */
-    size_t sem;      /* uint32 [B*H][N] semaphores                              */
+    size_t sem;      /* uint32 [B*H][N][4] semaphores (one per dQ-tile quarter)  */
     size_t D;        /* float  [B*H*S]                                          */
     size_t lse2;     /* float  [B*H*S] LSE * log2(e)                            */
     size_t dqacc;    /* float  [B*H*S][d]                                       */
