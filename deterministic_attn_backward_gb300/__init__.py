@@ -30,13 +30,16 @@ EXPORTED = (
     "dab_status_string", "dab_attn_bwd_ex", "dab_bwd_preprocess", "dab_bwd_workspace_layout",
     "dab_sched_units_per_head", "dab_sched_unit_steps", "dab_sched_step", "dab_sched_rank",
     "dab_sched_contributors", "dab_sched_gang_size", "dab_dag_simulate", "dab_dag_critical_path",
-    "dab_selftest_mma",
+    "dab_selftest_mma", "dab_last_error_string",
 )
 
 
 class DabError(RuntimeError):
     def __init__(self, code: int, what: str):
-        super().__init__(f"{what}: {STATUS.get(code, code)}")
+        detail = ""
+        if code == 4 and _lib is not None:
+            detail = " (" + _lib.dab_last_error_string().decode() + ")"
+        super().__init__(f"{what}: {STATUS.get(code, code)}{detail}")
         self.code = code
 
 
@@ -78,6 +81,8 @@ def load_library(path: str = LIB_PATH):
     lib.dab_check_status.restype = i
     lib.dab_status_string.argtypes = [i]
     lib.dab_status_string.restype = ctypes.c_char_p
+    lib.dab_last_error_string.argtypes = []
+    lib.dab_last_error_string.restype = ctypes.c_char_p
     lib.dab_sched_units_per_head.argtypes = [i, i, i]
     lib.dab_sched_units_per_head.restype = i
     lib.dab_sched_unit_steps.argtypes = [i, i, i, i]

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -42,6 +43,13 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
+thread_local char g_last_error[256] = "";
+
+// Record a failed CUDA call for dab_last_error_string() and map it.
+dab_status_t cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+  return DAB_ERR_CUDA;
+}
 
 // Per-device set-up: capability check and the dynamic shared-memory limits
 // of the kernels.  Returns false if the device cannot run them.
@@ -132,7 +140,7 @@ bool layout(int B, int H, int S, int d, dab_ws_layout_t* L) {
   L->status = off;
   off += 256;
   L->sem = off;
-  off = round_up(off + BH * N * 4 * 4, 256);  // 4 semaphores per dQ tile
+  off = round_up(off + BH * N * 8 * 4, 256);  // 8 semaphores per dQ tile
   L->D = off;
   off = round_up(off + rows * 4, 256);
   L->lse2 = off;
@@ -153,6 +161,8 @@ int elementwise_grid(int sms, long long work) {
 }  // namespace
 
 extern "C" {
+
+const char* dab_last_error_string(void) { return g_last_error; }
 
 const char* dab_status_string(dab_status_t s) {
   switch (s) {
@@ -211,7 +221,7 @@ dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v, void* o, 
     e = cudaLaunchKernel(dab::fwd_kernel_ptr<128>(), grid, block, args, dab::fwd_smem_bytes<128>(), stream);
   else
     e = cudaLaunchKernel(dab::fwd_kernel_ptr<64>(), grid, block, args, dab::fwd_smem_bytes<64>(), stream);
-  return e == cudaSuccess ? DAB_OK : DAB_ERR_CUDA;
+  return e == cudaSuccess ? DAB_OK : cuda_fail(e, "forward launch");
 }
 
 dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dout, int B, int H, int S,
@@ -227,14 +237,14 @@ dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dou
   if (!device_setup(nullptr, &sms)) return DAB_ERR_UNSUPPORTED;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const long long rows = (long long)B * H * S;
-  const int n_sem = B * H * (S / 128) * 4;
+  const int n_sem = B * H * (S / 128) * 8;
   float* dqacc = (sched == DAB_SCHED_ATOMIC) ? reinterpret_cast<float*>(ws + L.dqacc) : nullptr;
   const int grid = elementwise_grid(sms, rows * (d / 8));
   cudaError_t e = dab::launch_preprocess(
       d, o, dout, lse, reinterpret_cast<float*>(ws + L.D), reinterpret_cast<float*>(ws + L.lse2),
       reinterpret_cast<uint32_t*>(ws + L.sem), n_sem, reinterpret_cast<dab::WsHeader*>(ws + L.status),
       dqacc, rows * d, (int)rows, grid, stream);
-  return e == cudaSuccess ? DAB_OK : DAB_ERR_CUDA;
+  return e == cudaSuccess ? DAB_OK : cuda_fail(e, "preprocess launch");
 }
 
 dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
@@ -300,7 +310,7 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(448);
+  cfg.blockDim = dim3(640);
   cfg.dynamicSmemBytes = (d == 128) ? dab::bwd_smem_bytes<128>() : dab::bwd_smem_bytes<64>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -311,12 +321,12 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
   void* args[] = {&p};
   cudaError_t e = cudaLaunchKernelExC(&cfg, d == 128 ? dab::bwd_kernel_ptr<128>() : dab::bwd_kernel_ptr<64>(),
                                       args);
-  if (e != cudaSuccess) return DAB_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e, "main kernel launch");
 
   if (!(flags & DAB_BWD_SKIP_CONVERT)) {
     const long long elems = rows * d;
     e = dab::launch_convert(p.dqacc, dq, elems, scale, elementwise_grid(sms, elems / 4), stream);
-    if (e != cudaSuccess) return DAB_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail(e, "convert launch");
   }
   return DAB_OK;
 }

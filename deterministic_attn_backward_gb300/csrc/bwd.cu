@@ -16,16 +16,16 @@
 // written once at its end.  The dQ partial is added to an f32 accumulator in
 // global memory by the reducer warps: for the deterministic schedules in the
 // fixed order rank(i, j) (technical summary section 1: a fixed accumulation
-// order for dQ), waiting on per-(head, Q tile, quarter) semaphores with acquire loads
+// order for dQ), waiting on per-(head, Q tile, eighth) semaphores with acquire loads
 // and publishing with a release store; for ATOMIC with unordered float adds.
 //
-// Warp roles (14 warps):
+// Warp roles (20 warps):
 //   warp 0      TMA producer (K_i, V_i per chain; Q_j, dO_j, LSE_j, D_j per
 //               step, double-buffered) and tensor-memory allocation
 //   warp 1      MMA issuer (one thread)
-//   warps 2-9   softmax / dS, two groups of four warps, 64 Q columns each
-//               (thread = KV row), and the chain epilogue (dV / dK)
-//   warps 10-13 dQ reducer, one quarter of the dQ tile and one semaphore each
+//   warps 4-11  softmax / dS, two warpgroups of 64 Q columns each (thread =
+//               KV row), and the chain epilogue (dV by one, dK by the other)
+//   warps 12-19 dQ reducer, one eighth of the dQ tile and one semaphore each
 // Every wait is bounded: on expiry the kernel records DAB_ERR_TIMEOUT in the
 // workspace and every role drains and returns.
 #include <cuda.h>
@@ -39,10 +39,11 @@
 namespace dab {
 namespace {
 
-constexpr int kThreads = 448;       // 14 warps (launch configuration; 144 registers each)
-constexpr int kSoftmaxWarp0 = 2;    // warps 2-5: columns 0-63, warps 6-9: columns 64-127
-constexpr int kReducerWarp0 = 10;   // warps 10-13
-constexpr int kSubTiles = 4;        // dQ tile = 4 sub-tiles, one semaphore and reducer warp each
+// 20 warps: five per SM sub-partition, 96 registers per thread.
+constexpr int kThreads = 640;
+constexpr int kSoftmaxWarp0 = 4;    // warps 4-7: Q columns 0-63, warps 8-11: 64-127
+constexpr int kReducerWarp0 = 12;   // warps 12-19: two reducer warpgroups
+constexpr int kSubTiles = 8;        // dQ tile = 8 sub-tiles, one semaphore and reducer warp each
 
 template <int HD>
 struct Cfg {
@@ -112,7 +113,7 @@ static __device__ __noinline__ bool sem_wait(const uint32_t* sem, uint32_t targe
 }
 
 template <int HD>
-__global__ void __maxnreg__(144) bwd_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = Cfg<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
@@ -136,7 +137,7 @@ __global__ void __maxnreg__(144) bwd_kernel(const __grid_constant__ BwdParams p)
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1 + 8);
       mbar_init(&bars->unit_full[s], 1);
-      mbar_init(&bars->unit_empty[s], 1 + 8 + 4);
+      mbar_init(&bars->unit_empty[s], 1 + 8 + 8);
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
@@ -145,7 +146,7 @@ __global__ void __maxnreg__(144) bwd_kernel(const __grid_constant__ BwdParams p)
     mbar_init(&bars->dv_done, 1);
     mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_empty, 4);
+    mbar_init(&bars->dq_empty, 8);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
@@ -364,13 +365,13 @@ __global__ void __maxnreg__(144) bwd_kernel(const __grid_constant__ BwdParams p)
         // over the columns this warpgroup has just read.
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tbase + lane_off + C::kColS + 64 * h + 32 * c, v);
-          uint32_t w16[16];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[16];
+          tmem_ld16(tbase + lane_off + C::kColS + 64 * h + 16 * c, v);
+          uint32_t w8[8];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int col = 32 * c + e;          // column within this half
+          for (int e = 0; e < 16; e += 2) {
+            const int col = 16 * c + e;          // column within this half
             float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2e, -lse[col]));
             float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2e, -lse[col + 1]));
             if (diag) {
@@ -378,10 +379,10 @@ __global__ void __maxnreg__(144) bwd_kernel(const __grid_constant__ BwdParams p)
               if (r > qc) p0 = 0.f;
               if (r > qc + 1) p1 = 0.f;
             }
-            w16[e >> 1] = pack_bf16x2(p0, p1);
-            pk[16 * c + (e >> 1)] = w16[e >> 1];
+            w8[e >> 1] = pack_bf16x2(p0, p1);
+            pk[8 * c + (e >> 1)] = w8[e >> 1];
           }
-          tmem_st16(tbase + lane_off + C::kColS + 64 * h + 16 * c, w16);
+          tmem_st8(tbase + lane_off + C::kColS + 64 * h + 8 * c, w8);
         }
         tc_fence_before();
         __syncwarp();
@@ -391,26 +392,26 @@ __global__ void __maxnreg__(144) bwd_kernel(const __grid_constant__ BwdParams p)
         if (s > 0 && !warp_wait(&bars->ds_free, (s - 1) & 1, wc, 34)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tbase + lane_off + C::kColDP + 64 * h + 32 * c, v);
-          uint32_t w16[16];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[16];
+          tmem_ld16(tbase + lane_off + C::kColDP + 64 * h + 16 * c, v);
+          uint32_t w8[8];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int col = 32 * c + e;
-            const uint32_t pp = pk[16 * c + (e >> 1)];
+          for (int e = 0; e < 16; e += 2) {
+            const int col = 16 * c + e;
+            const uint32_t pp = pk[8 * c + (e >> 1)];
             const float p0 = __uint_as_float(pp << 16);
             const float p1 = __uint_as_float(pp & 0xFFFF0000u);
             const float ds0 = p0 * (__uint_as_float(v[e]) - dd[col]);
             const float ds1 = p1 * (__uint_as_float(v[e + 1]) - dd[col + 1]);
-            w16[e >> 1] = pack_bf16x2(ds0, ds1);
+            w8[e >> 1] = pack_bf16x2(ds0, ds1);
           }
           uint8_t* rowp = sds + r * 128;
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int cc = c * 4 + m;
+          for (int m = 0; m < 2; ++m) {
+            const int cc = c * 2 + m;            // 16-byte chunk of the 128-byte row
             *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) =
-                make_uint4(w16[4 * m], w16[4 * m + 1], w16[4 * m + 2], w16[4 * m + 3]);
+                make_uint4(w8[4 * m], w8[4 * m + 1], w8[4 * m + 2], w8[4 * m + 3]);
           }
         }
         fence_proxy_async_smem();
@@ -430,12 +431,12 @@ __global__ void __maxnreg__(144) bwd_kernel(const __grid_constant__ BwdParams p)
           const uint32_t col0 = (h == 0) ? C::kColDV : C::kColDK;
           const float sc = (h == 0) ? 1.0f : p.scale;
 #pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tbase + lane_off + col0 + 32 * c, v);
-            uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+          for (int c = 0; c < HD / 16; ++c) {
+            uint32_t v[16];
+            tmem_ld16(tbase + lane_off + col0 + 16 * c, v);
+            uint4* dst = reinterpret_cast<uint4*>(out + 16 * c);
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int m = 0; m < 2; ++m)
               dst[m] = make_uint4(
                   pack_bf16x2(sc * __uint_as_float(v[8 * m]), sc * __uint_as_float(v[8 * m + 1])),
                   pack_bf16x2(sc * __uint_as_float(v[8 * m + 2]), sc * __uint_as_float(v[8 * m + 3])),
@@ -452,17 +453,21 @@ __global__ void __maxnreg__(144) bwd_kernel(const __grid_constant__ BwdParams p)
     }
   } else if (warp >= kReducerWarp0) {
     // ------------------------------------------------------ dQ reducer
-    // Four warps.  Each drains its tensor-memory quadrant of the dQ partial
-    // into registers at once (so the tensor memory is free for the next
-    // partial), then adds its fixed quarter of the tile into the f32
-    // accumulator: d columns 32w..32w+31 of all 128 Q rows for d = 128
-    // (dQ^T: lanes = d), Q rows 32w..32w+31 for d = 64 (dQ: lanes = Q rows).
-    // For the ordered schedules every quarter has its own semaphore, so
-    // consecutive contributors to one dQ tile overlap on different quarters
+    // Two warpgroups, eight warps.  Warp (half, quad) drains its half of its
+    // tensor-memory quadrant of the dQ partial into registers at once (so
+    // the tensor memory is free for the next partial), then adds that
+    // eighth of the tile into the f32 accumulator:
+    //   d = 128 (dQ^T, lanes = d):  d columns 32*quad.., Q rows 64*half..+63
+    //   d =  64 (dQ, lanes = Q rows): Q rows 32*quad.., d columns 32*half..+31
+    // For the ordered schedules every eighth has its own semaphore, so
+    // consecutive contributors to one dQ tile overlap on different eighths
     // while each element still receives its partial sums in rank order.
-    const int quad = warp & 3;       // tensor-memory lane quadrant = sub-tile
-    const int r = quad * 32 + lane;  // d index (d = 128) or Q row (d = 64)
+    const int quad = warp & 3;                          // tensor-memory lane quadrant
+    const int half = (warp - kReducerWarp0) >> 2;
+    const int sub = half * 4 + quad;                    // sub-tile / semaphore index
+    const int r = quad * 32 + lane;                     // d index (d = 128) or Q row (d = 64)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    constexpr int kVals = (HD == 128) ? 64 : 32;        // values per thread per step
     int s = 0, uidx = 0;
     bool ok = true;
     while (ok) {
@@ -479,19 +484,19 @@ __global__ void __maxnreg__(144) bwd_kernel(const __grid_constant__ BwdParams p)
         const Step st = step(p.sched, p.mask, p.N, u, t);
         // everything but the values is computed before the drain
         const int rank = deterministic ? dab::rank(p.sched, p.mask, p.N, st.kv, st.q) : 0;
-        uint32_t* sem = p.sem + ((size_t)bh * p.N + st.q) * kSubTiles + quad;
-        const uint32_t sem_detail = (uint32_t)((bh * p.N + st.q) * kSubTiles + quad);
+        uint32_t* sem = p.sem + ((size_t)bh * p.N + st.q) * kSubTiles + sub;
+        const uint32_t sem_detail = (uint32_t)((bh * p.N + st.q) * kSubTiles + sub);
         const bool store = deterministic && rank == 0;  // the first contribution overwrites
         const size_t row0 = (size_t)bh * p.S + (size_t)st.q * kTile;
-        float* base = (HD == 128) ? p.dqacc + row0 * HD + r        // column r of Q rows 0..127
-                                  : p.dqacc + (row0 + (size_t)r) * HD;  // Q row r, d 0..63
+        float* base = (HD == 128) ? p.dqacc + (row0 + (size_t)half * 64) * HD + r
+                                  : p.dqacc + (row0 + (size_t)r) * HD + half * 32;
         if (!warp_wait(&bars->dq_full, s & 1, wc, 41)) { ok = false; break; }
         tc_fence_after();
-        constexpr int kVals = (HD == 128) ? 128 : 64;
         uint32_t v[kVals];
 #pragma unroll
         for (int c = 0; c < kVals / 32; ++c)
-          tmem_ld32(tbase + lane_off + C::kColDQ + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+          tmem_ld32(tbase + lane_off + C::kColDQ + (uint32_t)(half * kVals + 32 * c),
+                    *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->dq_empty);
@@ -504,14 +509,14 @@ __global__ void __maxnreg__(144) bwd_kernel(const __grid_constant__ BwdParams p)
         if (HD == 128) {
           if (store) {
 #pragma unroll
-            for (int q = 0; q < 128; ++q) base[(size_t)q * HD] = __uint_as_float(v[q]);
+            for (int q = 0; q < 64; ++q) base[(size_t)q * HD] = __uint_as_float(v[q]);
           } else {
 #pragma unroll
-            for (int q = 0; q < 128; ++q) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
+            for (int q = 0; q < 64; ++q) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
           }
         } else {
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
+          for (int m = 0; m < 8; ++m) {
             const float a0 = __uint_as_float(v[4 * m]), a1 = __uint_as_float(v[4 * m + 1]);
             const float a2 = __uint_as_float(v[4 * m + 2]), a3 = __uint_as_float(v[4 * m + 3]);
             if (store)

@@ -56,8 +56,9 @@ typedef enum {
  *   SERIAL        KV tile i walks its Q tiles in ascending order; dQ_j gathers
  *                 its partial sums in ascending KV order (rank(i, j) = i).
  *                 The serialised deterministic baseline (DASH summary sec. 1).
- *   DESCENDING_Q  Same reduction order as SERIAL, Q tiles walked from the last
- *                 one down (DASH summary sec. 2.2.A).  Bitwise equal to SERIAL.
+ *   DESCENDING_Q  Same dQ reduction order as SERIAL, Q tiles walked from the
+ *                 last one down (DASH summary sec. 2.2.A).  dQ is bitwise equal
+ *                 to SERIAL's; dK and dV accumulate along the reversed walk.
  *   SHIFT         Full mask: KV tile i walks Q tiles i, i+1, ..., N-1, 0, ...,
  *                 i-1 and dQ_j is reduced in visit order (DASH summary
  *                 sec. 2.2.B).  Causal mask: the symmetric variant, where one
@@ -95,9 +96,8 @@ dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v,
 
 /* Bytes of device workspace that dab_attn_bwd needs for this problem (0 on
  * invalid arguments).  The workspace holds the status word, the dispatch
- * counter, four semaphores per 128-row dQ tile (one per quarter), D and
- * LSE*log2(e) per row, and
- * the float32 dQ accumulator [B][H][S][d].  It needs no initialisation: the
+ * counter, eight semaphores per 128-row dQ tile (one per eighth), D and
+ * LSE*log2(e) per row, and the float32 dQ accumulator [B][H][S][d].  It needs no initialisation: the
  * first kernel of every backward call resets what must start at zero.      */
 size_t dab_bwd_workspace_size(int B, int H, int S, int d,
                               dab_mask_t mask, dab_sched_t sched);
@@ -129,6 +129,11 @@ dab_status_t dab_check_status(const void* workspace, cudaStream_t stream);
 
 /* Static, human-readable name of a status code.                             */
 const char* dab_status_string(dab_status_t status);
+
+/* The CUDA error behind the calling thread's last DAB_ERR_CUDA (the failing
+ * step, the CUDA error name and number), or "" if there was none.  The
+ * string is owned by the library and valid until the next call that fails. */
+const char* dab_last_error_string(void);
 
 /* ------------------------------------------------------------------------ */
 /* Extended backward options.  dab_attn_bwd() is dab_attn_bwd_ex() with
@@ -165,7 +170,7 @@ dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dou
 /* Byte offsets of the workspace regions (for tests and tools).             */
 typedef struct {
     size_t status;   /* uint32 status word, uint32 error detail, uint32 counter */
-    size_t sem;      /* uint32 [B*H][N][4] semaphores (one per dQ-tile quarter)  */
+    size_t sem;      /* uint32 [B*H][N][8] semaphores (one per dQ-tile eighth)   */
     size_t D;        /* float  [B*H*S]                                          */
     size_t lse2;     /* float  [B*H*S] LSE * log2(e)                            */
     size_t dqacc;    /* float  [B*H*S][d]                                       */

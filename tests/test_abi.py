@@ -49,7 +49,7 @@ def test_workspace_layout(lib):
     L = dab.workspace_layout(B, H, S, d, "causal", "descending_q")
     rows = B * H * S
     assert L.status == 0 and L.sem == 256
-    assert L.D >= L.sem + 16 * B * H * (S // 128)
+    assert L.D >= L.sem + 32 * B * H * (S // 128)
     assert L.lse2 >= L.D + 4 * rows and L.dqacc >= L.lse2 + 4 * rows
     assert L.total >= L.dqacc + 4 * rows * d
     for off in (L.sem, L.D, L.lse2, L.dqacc, L.total):
