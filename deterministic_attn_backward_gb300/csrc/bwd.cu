@@ -365,24 +365,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         // over the columns this warpgroup has just read.
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[16];
-          tmem_ld16(tbase + lane_off + C::kColS + 64 * h + 16 * c, v);
-          uint32_t w8[8];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_off + C::kColS + 64 * h + 32 * c, v);
+          uint32_t w16[16];
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const int col = 16 * c + e;          // column within this half
-            float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2e, -lse[col]));
-            float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2e, -lse[col + 1]));
+          for (int e = 0; e < 32; e += 4) {
+            const int col = 32 * c + e;          // column within this half
+            const float4 l4 = *reinterpret_cast<const float4*>(lse + col);
+            float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2e, -l4.x));
+            float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2e, -l4.y));
+            float p2 = ex2_approx(fmaf(__uint_as_float(v[e + 2]), p.scale_log2e, -l4.z));
+            float p3 = ex2_approx(fmaf(__uint_as_float(v[e + 3]), p.scale_log2e, -l4.w));
             if (diag) {
               const int qc = 64 * h + col;       // Q column within the tile
               if (r > qc) p0 = 0.f;
               if (r > qc + 1) p1 = 0.f;
+              if (r > qc + 2) p2 = 0.f;
+              if (r > qc + 3) p3 = 0.f;
             }
-            w8[e >> 1] = pack_bf16x2(p0, p1);
-            pk[8 * c + (e >> 1)] = w8[e >> 1];
+            w16[e >> 1] = pack_bf16x2(p0, p1);
+            w16[(e >> 1) + 1] = pack_bf16x2(p2, p3);
+            pk[16 * c + (e >> 1)] = w16[e >> 1];
+            pk[16 * c + (e >> 1) + 1] = w16[(e >> 1) + 1];
           }
-          tmem_st8(tbase + lane_off + C::kColS + 64 * h + 8 * c, w8);
+          tmem_st16(tbase + lane_off + C::kColS + 64 * h + 16 * c, w16);
         }
         tc_fence_before();
         __syncwarp();
@@ -397,14 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           tmem_ld16(tbase + lane_off + C::kColDP + 64 * h + 16 * c, v);
           uint32_t w8[8];
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
+          for (int e = 0; e < 16; e += 4) {
             const int col = 16 * c + e;
-            const uint32_t pp = pk[8 * c + (e >> 1)];
-            const float p0 = __uint_as_float(pp << 16);
-            const float p1 = __uint_as_float(pp & 0xFFFF0000u);
-            const float ds0 = p0 * (__uint_as_float(v[e]) - dd[col]);
-            const float ds1 = p1 * (__uint_as_float(v[e + 1]) - dd[col + 1]);
+            const float4 d4 = *reinterpret_cast<const float4*>(dd + col);
+            const uint32_t pa = pk[8 * c + (e >> 1)], pb = pk[8 * c + (e >> 1) + 1];
+            const float ds0 = __uint_as_float(pa << 16) * (__uint_as_float(v[e]) - d4.x);
+            const float ds1 = __uint_as_float(pa & 0xFFFF0000u) * (__uint_as_float(v[e + 1]) - d4.y);
+            const float ds2 = __uint_as_float(pb << 16) * (__uint_as_float(v[e + 2]) - d4.z);
+            const float ds3 = __uint_as_float(pb & 0xFFFF0000u) * (__uint_as_float(v[e + 3]) - d4.w);
             w8[e >> 1] = pack_bf16x2(ds0, ds1);
+            w8[(e >> 1) + 1] = pack_bf16x2(ds2, ds3);
           }
           uint8_t* rowp = sds + r * 128;
 #pragma unroll
