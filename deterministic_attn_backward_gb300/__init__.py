@@ -269,7 +269,7 @@ def selftest_mma(d: int, x, y, z, pm):
     out0 = torch.empty((128, 128), dtype=torch.float32, device=dev)
     out1 = torch.empty((128, d), dtype=torch.float32, device=dev)
     out2 = torch.empty((128, d), dtype=torch.float32, device=dev)
-    out3 = torch.empty((128, d), dtype=torch.float32, device=dev)
+    out3 = torch.empty((128, 128 if d == 128 else 64), dtype=torch.float32, device=dev)
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)
     _check(lib.dab_selftest_mma(d, x.data_ptr(), y.data_ptr(), z.data_ptr(), pm.data_ptr(),
                                 out0.data_ptr(), out1.data_ptr(), out2.data_ptr(), out3.data_ptr(),

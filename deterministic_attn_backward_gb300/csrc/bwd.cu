@@ -10,7 +10,7 @@
 //     dV_i += P^T dO_j                      (P^T read from tensor memory)
 //     dS^T = P^T o (dP^T - D_j)             (softmax warps -> shared memory)
 //     dK_i += dS^T Q_j
-//     dQ_j partial = dS K_i
+//     dQ_j partial = dS K_i                 (as dQ^T = K_i^T dS^T for d = 128)
 // dK_i and dV_i stay in tensor memory for the whole chain (the KV-chain
 // constraint of the DASH DAG model, technical summary section 2.1) and are
 // written once at its end.  The dQ partial is added to an f32 accumulator in
@@ -68,7 +68,8 @@ struct Cfg {
   // Instruction descriptors.
   static constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
   static constexpr uint32_t kIdAcc = idesc_bf16(128, HD, 0, 1);  // dV, dK
-  static constexpr uint32_t kIdDQ = idesc_bf16(128, HD, 1, 1);                 // dQ = dS K
+  static constexpr uint32_t kIdDQ = (HD == 128) ? idesc_bf16(128, 128, 1, 1)   // dQ^T
+                                                : idesc_bf16(128, 64, 1, 1);   // dQ
 };
 
 struct Bars {
@@ -286,13 +287,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             mma_ts(tbase + C::kColDV, tbase + C::kColS + (k >> 2) * 64 + (k & 3) * 8,
                    desc_mnmajor(sDO, k, 128), C::kIdAcc, !(st.chain_first && k == 0));
           mma_commit(&bars->dv_done);
-          // dQ partial = dS K (A = dS, B = K, both MN-major; lanes = Q rows)
+          // dQ partial (d = 128: dQ^T = K^T dS^T; d = 64: dQ = dS K)
           if (!mbar_wait(&bars->ds_full, s & 1, wc, 17)) { ok = false; break; }
           if (HD == 64 && s > 0 && !mbar_wait(&bars->dq_empty, (s - 1) & 1, wc, 18)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)
-            mma_ss(tbase + C::kColDQ, desc_mnmajor(sDS, k, 128), desc_mnmajor(sK, k, 128), C::kIdDQ, k > 0);
+          for (int k = 0; k < kTile / 16; ++k) {
+            const uint64_t a = (HD == 128) ? desc_mnmajor(sK, k, 128) : desc_mnmajor(sDS, k, 128);
+            const uint64_t b = (HD == 128) ? desc_mnmajor(sDS, k, 128) : desc_mnmajor(sK, k, 128);
+            mma_ss(tbase + C::kColDQ, a, b, C::kIdDQ, k > 0);
+          }
           mma_commit(&bars->dq_full);
           const bool next = !st.chain_last;  // the next step continues this chain
           if (next) {
@@ -458,21 +462,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp >= kReducerWarp0) {
     // ------------------------------------------------------ dQ reducer
-    // Two warpgroups, eight warps.  The dQ partial sits in tensor memory with
-    // one Q row per lane.  Warp (half, quad) drains Q rows 32*quad..+31,
-    // d columns half*HD/2 .. +HD/2-1 into registers at once (so the tensor
-    // memory is free for the next partial), then adds that eighth of the tile
-    // into the f32 accumulator with 16-byte vector adds (few memory
-    // instructions, so that they do not crowd out the softmax warps' shared
-    // loads).  For the ordered schedules every eighth has its own semaphore,
-    // so consecutive contributors to one dQ tile overlap on different eighths
+    // Two warpgroups, eight warps.  Warp (half, quad) drains its half of its
+    // tensor-memory quadrant of the dQ partial into registers at once (so
+    // the tensor memory is free for the next partial), then adds that
+    // eighth of the tile into the f32 accumulator:
+    //   d = 128 (dQ^T, lanes = d):  d columns 32*quad.., Q rows 64*half..+63
+    //   d =  64 (dQ, lanes = Q rows): Q rows 32*quad.., d columns 32*half..+31
+    // For the ordered schedules every eighth has its own semaphore, so
+    // consecutive contributors to one dQ tile overlap on different eighths
     // while each element still receives its partial sums in rank order.
     const int quad = warp & 3;                          // tensor-memory lane quadrant
     const int half = (warp - kReducerWarp0) >> 2;
     const int sub = half * 4 + quad;                    // sub-tile / semaphore index
-    const int r = quad * 32 + lane;                     // Q row of the tile
+    const int r = quad * 32 + lane;                     // d index (d = 128) or Q row (d = 64)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    constexpr int kVals = HD / 2;                       // values per thread per step
+    constexpr int kVals = (HD == 128) ? 64 : 32;        // values per thread per step
     int s = 0, uidx = 0;
     bool ok = true;
     while (ok) {
@@ -493,7 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         const uint32_t sem_detail = (uint32_t)((bh * p.N + st.q) * kSubTiles + sub);
         const bool store = deterministic && rank == 0;  // the first contribution overwrites
         const size_t row0 = (size_t)bh * p.S + (size_t)st.q * kTile;
-        float* base = p.dqacc + (row0 + (size_t)r) * HD + half * kVals;
+        float* base = (HD == 128) ? p.dqacc + (row0 + (size_t)half * 64) * HD + r
+                                  : p.dqacc + (row0 + (size_t)r) * HD + half * 32;
         if (!warp_wait(&bars->dq_full, s & 1, wc, 41)) { ok = false; break; }
         tc_fence_after();
         uint32_t v[kVals];
@@ -510,14 +515,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           g = __shfl_sync(0xffffffffu, g, 0);
           if (!g) { ok = false; break; }
         }
+        if (HD == 128) {
+          if (store) {
 #pragma unroll
-        for (int m = 0; m < kVals / 4; ++m) {
-          const float a0 = __uint_as_float(v[4 * m]), a1 = __uint_as_float(v[4 * m + 1]);
-          const float a2 = __uint_as_float(v[4 * m + 2]), a3 = __uint_as_float(v[4 * m + 3]);
-          if (store)
-            reinterpret_cast<float4*>(base)[m] = make_float4(a0, a1, a2, a3);
-          else
-            red_add_v4_f32(base + 4 * m, a0, a1, a2, a3);
+            for (int q = 0; q < 64; ++q) base[(size_t)q * HD] = __uint_as_float(v[q]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 64; ++q) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
+          }
+        } else {
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const float a0 = __uint_as_float(v[4 * m]), a1 = __uint_as_float(v[4 * m + 1]);
+            const float a2 = __uint_as_float(v[4 * m + 2]), a3 = __uint_as_float(v[4 * m + 3]);
+            if (store)
+              reinterpret_cast<float4*>(base)[m] = make_float4(a0, a1, a2, a3);
+            else
+              red_add_v4_f32(base + 4 * m, a0, a1, a2, a3);
+          }
         }
         if (deterministic) {
           // Publish: the warp's writes are ordered before the release of

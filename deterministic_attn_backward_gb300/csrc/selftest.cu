@@ -4,7 +4,7 @@
 //   out0 = X Y^T        A K-major smem, B K-major smem     (S^T, dP^T)
 //   out1 = P Y          A bf16 in tensor memory, B MN-major (dV)
 //   out2 = Z Y          A K-major (thread-written), B MN-major (dK)
-//   out3 = Z^T X        both MN-major                       (dQ)
+//   out3 = X^T Z  (d=128) / Z^T X (d=64)  both MN-major     (dQ^T / dQ)
 // X, Y: [128][d] bf16 (loaded by TMA); Z, P: [128][128] bf16 (written by
 // threads into the swizzled layout / into tensor memory).  Outputs f32.
 #include <cuda.h>
@@ -89,9 +89,14 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (ok) {
         tc_fence_after();
-        for (int k = 0; k < 8; ++k)
-          mma_ss(tb + kCol3, desc_mnmajor(sZ, k, 128), desc_mnmajor(sX, k, 128),
-                 idesc_bf16(128, HD, 1, 1), k > 0);
+        for (int k = 0; k < 8; ++k) {
+          if (HD == 128)
+            mma_ss(tb + kCol3, desc_mnmajor(sX, k, 128), desc_mnmajor(sZ, k, 128),
+                   idesc_bf16(128, 128, 1, 1), k > 0);
+          else
+            mma_ss(tb + kCol3, desc_mnmajor(sZ, k, 128), desc_mnmajor(sX, k, 128),
+                   idesc_bf16(128, 64, 1, 1), k > 0);
+        }
         mma_commit(&bars->mma_b);
       }
       mma_commit(&bars->drain);
@@ -137,7 +142,7 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) mbar_arrive(&bars->read_a);
       if (warp_wait(&bars->mma_b, 0, wc, 5)) {
         tc_fence_after();
-        constexpr int n3 = HD;
+        constexpr int n3 = (HD == 128) ? 128 : 64;
         for (int ch = 0; ch < n3 / 32; ++ch) {
           tmem_ld32(tb + lo + kCol3 + 32 * ch, v);
           for (int e = 0; e < 32; ++e) out3[r * n3 + 32 * ch + e] = __uint_as_float(v[e]);

@@ -22,7 +22,8 @@ extern "C" {
  *   out0   f32 [128][128]  = x y^T
  *   out1   f32 [128][d]    = pm y
  *   out2   f32 [128][d]    = z y
- *   out3   f32 [128][d]    = z^T x
+ *   out3   f32 [128][128]  = x^T z     (d = 128)
+ *          f32 [128][64]   = z^T x     (d = 64)
  *   status_ws  >= 256 bytes; its status word is read by dab_check_status().
  * Asynchronous on `stream`; argument errors are returned synchronously.     */
 dab_status_t dab_selftest_mma(int d, const void* x, const void* y, const void* z,
