@@ -236,19 +236,34 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     // dQ(s), and the tensor pipe always has work queued.  At a chain boundary
     // S and dP of the new chain's first step are issued once its K/V landed.
     if (lane == 0) {
-      const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sDS = sbase + C::kOffDS;
+      // Descriptors of every operand at K step 0, built once; step k adds a
+      // compile-time offset, so issuing an MMA costs almost no instructions
+      // (this thread shares its sub-partition with busy warps).
+      const uint64_t dK_k = desc_kmajor(sbase + C::kOffK, 0, 128);
+      const uint64_t dK_mn = desc_mnmajor(sbase + C::kOffK, 0, 128);
+      const uint64_t dV_k = desc_kmajor(sbase + C::kOffV, 0, 128);
+      const uint64_t dDS_k = desc_kmajor(sbase + C::kOffDS, 0, 128);
+      const uint64_t dDS_mn = desc_mnmajor(sbase + C::kOffDS, 0, 128);
+      // stage 1 lies one tile above stage 0: its descriptors differ by a constant
+      const uint64_t dQ_k0 = desc_kmajor(sbase + C::kOffQ, 0, 128);
+      const uint64_t dQ_mn0 = desc_mnmajor(sbase + C::kOffQ, 0, 128);
+      const uint64_t dDO_k0 = desc_kmajor(sbase + C::kOffDO, 0, 128);
+      const uint64_t dDO_mn0 = desc_mnmajor(sbase + C::kOffDO, 0, 128);
+      constexpr uint64_t kStageOff = C::kTileBytes >> 4;
+      const uint32_t tS = tbase + C::kColS, tDP = tbase + C::kColDP, tDV = tbase + C::kColDV;
+      const uint32_t tDK = tbase + C::kColDK, tDQ = tbase + C::kColDQ;
       auto issue_s = [&](int stage) {
-        const uint32_t sQ = sbase + C::kOffQ + stage * C::kTileBytes;
+        const uint64_t q0 = dQ_k0 + (uint64_t)stage * kStageOff;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tbase + C::kColS, desc_kmajor(sK, k, 128), desc_kmajor(sQ, k, 128), C::kIdS, k > 0);
+          mma_ss(tS, dK_k + koff_kmajor(k, 128), q0 + koff_kmajor(k, 128), C::kIdS, k > 0);
         mma_commit(&bars->s_full);
       };
       auto issue_dp = [&](int stage) {
-        const uint32_t sDO = sbase + C::kOffDO + stage * C::kTileBytes;
+        const uint64_t o0 = dDO_k0 + (uint64_t)stage * kStageOff;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tbase + C::kColDP, desc_kmajor(sV, k, 128), desc_kmajor(sDO, k, 128), C::kIdS, k > 0);
+          mma_ss(tDP, dV_k + koff_kmajor(k, 128), o0 + koff_kmajor(k, 128), C::kIdS, k > 0);
         mma_commit(&bars->dp_full);
       };
       int s = 0, chain = 0, uidx = 0;
@@ -265,8 +280,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         for (int t = 0; t < steps; ++t) {
           const Step st = step(p.sched, p.mask, p.N, u, t);
           const int stage = s & 1;
-          const uint32_t sQ = sbase + C::kOffQ + stage * C::kTileBytes;
-          const uint32_t sDO = sbase + C::kOffDO + stage * C::kTileBytes;
           if (!pre) {
             if (st.chain_first && !mbar_wait(&bars->kv_full, chain & 1, wc, 11)) { ok = false; break; }
             if (!mbar_wait(&bars->q_full[stage], (s >> 1) & 1, wc, 12)) { ok = false; break; }
@@ -282,10 +295,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           if (!mbar_wait(&bars->p_full, s & 1, wc, 15)) { ok = false; break; }
           if (st.chain_first && chain > 0 && !mbar_wait(&bars->acc_empty, (chain - 1) & 1, wc, 16)) { ok = false; break; }
           tc_fence_after();
+          {
+            const uint64_t o0 = dDO_mn0 + (uint64_t)stage * kStageOff;
+            const uint32_t acc0 = st.chain_first ? 0u : 1u;
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)
-            mma_ts(tbase + C::kColDV, tbase + C::kColS + (k >> 2) * 64 + (k & 3) * 8,
-                   desc_mnmajor(sDO, k, 128), C::kIdAcc, !(st.chain_first && k == 0));
+            for (int k = 0; k < kTile / 16; ++k)
+              mma_ts(tDV, tS + (k >> 2) * 64 + (k & 3) * 8, o0 + koff_mnmajor(k), C::kIdAcc,
+                     k == 0 ? acc0 : 1u);
+          }
           mma_commit(&bars->dv_done);
           // dQ partial (d = 128: dQ^T = K^T dS^T; d = 64: dQ = dS K)
           if (!mbar_wait(&bars->ds_full, s & 1, wc, 17)) { ok = false; break; }
@@ -293,9 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k) {
-            const uint64_t a = (HD == 128) ? desc_mnmajor(sK, k, 128) : desc_mnmajor(sDS, k, 128);
-            const uint64_t b = (HD == 128) ? desc_mnmajor(sDS, k, 128) : desc_mnmajor(sK, k, 128);
-            mma_ss(tbase + C::kColDQ, a, b, C::kIdDQ, k > 0);
+            const uint64_t a = ((HD == 128) ? dK_mn : dDS_mn) + koff_mnmajor(k);
+            const uint64_t b = ((HD == 128) ? dDS_mn : dK_mn) + koff_mnmajor(k);
+            mma_ss(tDQ, a, b, C::kIdDQ, k > 0);
           }
           mma_commit(&bars->dq_full);
           const bool next = !st.chain_last;  // the next step continues this chain
@@ -307,10 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             issue_s(st1);
           }
           // dK += dS^T Q
+          {
+            const uint64_t q0 = dQ_mn0 + (uint64_t)stage * kStageOff;
+            const uint32_t acc0 = st.chain_first ? 0u : 1u;
 #pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)
-            mma_ss(tbase + C::kColDK, desc_kmajor(sDS, k, 128), desc_mnmajor(sQ, k, 128), C::kIdAcc,
-                   !(st.chain_first && k == 0));
+            for (int k = 0; k < kTile / 16; ++k)
+              mma_ss(tDK, dDS_k + koff_kmajor(k, 128), q0 + koff_mnmajor(k), C::kIdAcc, k == 0 ? acc0 : 1u);
+          }
           mma_commit(&bars->q_empty[stage]);
           mma_commit(&bars->ds_free);
           if (st.chain_last) {

@@ -122,6 +122,16 @@ static __device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, W
   }
 }
 
+// Start-address offset, in the descriptor's 16-byte units, of K step k of a
+// K-major operand with `rows` rows (64-column blocks), and of an MN-major
+// operand (16 K rows of 128 bytes per step).  Adding them to a descriptor
+// built for k = 0 gives the descriptor of step k (the start address is the
+// low field and never carries into the next one for shared addresses).
+__host__ __device__ constexpr uint64_t koff_kmajor(int k, int rows) {
+  return (uint64_t)(((k >> 2) * rows * 128 + (k & 3) * 32) >> 4);
+}
+__host__ __device__ constexpr uint64_t koff_mnmajor(int k) { return (uint64_t)((k * 2048) >> 4); }
+
 // K-major operand: rows x (64-column blocks); K step k (16 elements).
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int k, int rows) {
   return sdesc_sw128(base + (k >> 2) * rows * 128 + (k & 3) * 32, 16, 1024);
