@@ -30,7 +30,7 @@ EXPORTED = (
     "dab_status_string", "dab_attn_bwd_ex", "dab_bwd_preprocess", "dab_bwd_workspace_layout",
     "dab_sched_units_per_head", "dab_sched_unit_steps", "dab_sched_step", "dab_sched_rank",
     "dab_sched_contributors", "dab_sched_gang_size", "dab_dag_simulate", "dab_dag_critical_path",
-    "dab_selftest_mma", "dab_last_error_string",
+    "dab_selftest_mma", "dab_last_error_string", "dab_attn_bwd_noalloc",
 )
 
 
@@ -101,6 +101,8 @@ def load_library(path: str = LIB_PATH):
     lib.dab_dag_simulate.restype = i
     lib.dab_dag_critical_path.argtypes = [i, i, i, ctypes.c_double, ctypes.c_double, i]
     lib.dab_dag_critical_path.restype = ctypes.c_double
+    lib.dab_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 4 + [f, i, i, vp]
+    lib.dab_attn_bwd_noalloc.restype = i
     lib.dab_selftest_mma.argtypes = [i] + [vp] * 10
     lib.dab_selftest_mma.restype = i
     _lib = lib

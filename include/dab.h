@@ -182,6 +182,43 @@ dab_status_t dab_bwd_workspace_layout(int B, int H, int S, int d,
                                       dab_ws_layout_t* layout);
 
 /* ------------------------------------------------------------------------ */
+/* The backward for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point.  Some callers may not
+ * call cudaMalloc where they need the backward -- for example a plugin inside
+ * a host framework that owns and budgets all device memory, or a
+ * latency-critical loop where an allocation, which can synchronise the
+ * device, is not acceptable -- and so cannot provide the workspace that
+ * dab_attn_bwd needs.  dab_attn_bwd_noalloc is dab_attn_bwd with that
+ * workspace taken from a fixed array inside the library
+ * (DAB_NOALLOC_SCRATCH_BYTES bytes; every GPU that loads the library holds it
+ * until the process exits).  The caller still passes every input and output.
+ *
+ *   Limit    problems whose dab_bwd_workspace_size() exceeds
+ *            DAB_NOALLOC_SCRATCH_BYTES are rejected with DAB_ERR_WORKSPACE
+ *            before anything is launched (roughly B*H*S*d <= 8M elements).
+ *   Set-up   the first call on a device, with that device current, looks up
+ *            the array's device address (cudaGetSymbolAddress) and caches
+ *            it; make that first call before any stream capture.  A failed
+ *            lookup returns DAB_ERR_CUDA.
+ *   Sharing  every call on a device uses the same array, which keeps the
+ *            last call's contents; each call's first kernel clears what must
+ *            start at zero.  Calls whose kernels overlap on the GPU (for
+ *            instance on two streams) race on the array: serialise them.
+ *   Status   the device status word lives in the array too, so
+ *            dab_check_status() cannot be pointed at it; a device-side
+ *            timeout leaves the gradients undefined.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.    */
+#define DAB_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+dab_status_t dab_attn_bwd_noalloc(const void* q, const void* k, const void* v,
+                                  const void* o, const float* lse, const void* dout,
+                                  void* dq, void* dk, void* dv,
+                                  int B, int H, int S, int d, float scale,
+                                  dab_mask_t mask, dab_sched_t sched,
+                                  cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Schedule introspection (host only, no GPU needed).  N = S/128 tiles.
  * These are the same functions the main kernel evaluates on the device.     */
 
