@@ -3,7 +3,8 @@
 One step = one pass of the whole backward hot path (preprocess, main kernel,
 dQ convert) over the workload B=2, H=16, S=8192, d=128 with the causal mask
 (Q and K scaled by 0.5, seed 2) and again with the full mask at the same
-shape, each with its deterministic schedule.  FLOPs: 10*B*H*S^2*d for the full
+shape, each with the fastest of the three deterministic schedules in this
+run's per-schedule table (named in `config.schedules`).  FLOPs: 10*B*H*S^2*d for the full
 mask, half for causal (exp, preprocess and convert not counted).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -30,8 +31,16 @@ METRIC = "deterministic attn-bwd TFLOP/s (causal+full) and % of GB300 dense BF16
 UNIT = "TFLOP/s"
 B, H, S, D = 2, 16, 8192, 128
 SEED, QK_SCALE = 2, 0.5
-STEP_SCHEDS = {"causal": "descending_q", "full": "shift"}  # the schedules one step runs
 ALL_SCHEDS = ("serial", "descending_q", "shift", "atomic")
+DET_SCHEDS = ("serial", "descending_q", "shift")
+
+# DRAM bytes (read + write) of one main-kernel launch of this workload, from an
+# ncu capture (profiles/bwd_main_*.md: B=1 launches, traffic scales with the
+# number of heads, so x2), keyed by the SHA-1 of the kernel source it was
+# taken on.  Reported only while the source is unchanged.
+TRAFFIC_CAPTURES = {
+    "36b2d414e2c6559f2744729c64f6e247bee98634": 2 * ((136.133888 + 89.668096) + (138.070784 + 88.849152)) / 2 * 1e6,
+}
 MASKS = ("causal", "full")
 
 
@@ -54,6 +63,15 @@ def load_peaks() -> dict:
     except (OSError, KeyError, ValueError):
         return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "bf16_tflops_sustained": 1700.0,
                 "source": "fallback"}
+
+
+def traffic_for_current_kernel():
+    import hashlib
+    path = os.path.join(ROOT, "deterministic_attn_backward_gb300", "csrc", "bwd.cu")
+    with open(path, "rb") as f:
+        h = hashlib.sha1(f.read()).hexdigest()
+    t = TRAFFIC_CAPTURES.get(h)
+    return round(t) if t is not None else None
 
 
 def max_over_ranks(value: float, world: int, device=None) -> float:
@@ -150,9 +168,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         o, lse = fwd[mask]
         dab.attn_bwd(qd, kd, vd, o, lse, dod, mask, sched, workspace=ws[mask], out=outs[mask])
 
+    step_scheds = {"causal": "shift", "full": "shift"}  # replaced by the fastest below
+
     def step():
         for m in MASKS:
-            bwd(m, STEP_SCHEDS[m])
+            bwd(m, step_scheds[m])
 
     def barrier():
         if world > 1:
@@ -187,6 +207,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             ms = e0.elapsed_time(e1) / reps
             per[m][sched] = {"ms": round(ms, 4), "tflops": round(flops(m) / ms / 1e9, 2)}
         check()
+        # a step runs, per mask, the fastest deterministic schedule
+        step_scheds[m] = min(DET_SCHEDS, key=lambda x: per[m][x]["ms"])
         ts, ta = per[m]["serial"]["ms"], per[m]["atomic"]["ms"]
         for sched in ("descending_q", "shift"):
             gap = ts - ta
@@ -199,7 +221,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     main_ms = {}
     for m in MASKS:
         o, lse = fwd[m]
-        sched = STEP_SCHEDS[m]
+        sched = step_scheds[m]
         tot, reps = 0.0, 10
         for it in range(reps + 3):
             dab.bwd_preprocess(o, lse, dod, m, sched, ws[m])
@@ -243,7 +265,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             for hd, dd in zip(host_in[m], dev_in[m]):
                 dd.copy_(hd, non_blocking=True)
             qq, kk, vv, oo, ll, gg = dev_in[m]
-            dab.attn_bwd(qq, kk, vv, oo, ll, gg, m, STEP_SCHEDS[m], workspace=ws[m], out=outs[m])
+            dab.attn_bwd(qq, kk, vv, oo, ll, gg, m, step_scheds[m], workspace=ws[m], out=outs[m])
             for dd, hh in zip(outs[m], host_out[m]):
                 hh.copy_(dd, non_blocking=True)
 
@@ -276,13 +298,14 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": workload_name(), "B": B, "H": H, "S": S, "d": D,
-                   "masks": list(MASKS), "schedules": STEP_SCHEDS, "seed": SEED,
+                   "masks": list(MASKS), "schedules": step_scheds, "seed": SEED,
                    "qk_scale": QK_SCALE,
                    "l2": "inputs exceed L2 (5 x 64 MiB read per call), no flush",
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": round(value / world / peak, 4),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic_for_current_kernel(),
                      "kernel": "bwd_kernel<128>", "peak_source": peaks["source"] + " (burst)",
                      "launch_ms": {m: round(x, 4) for m, x in main_ms.items()}},
         "per_schedule": per,
