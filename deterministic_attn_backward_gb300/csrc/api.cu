@@ -26,7 +26,8 @@ template <int HD> const void* selftest_kernel_ptr();
 cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const float* lse, float* D,
                               float* lse2, uint32_t* sem, int n_sem, WsHeader* hdr, float* dqacc,
                               long long dq_elems, int rows, int grid, cudaStream_t stream);
-cudaError_t launch_convert(const float* dqacc, void* dq, long long elems, float scale, int grid,
+cudaError_t launch_convert(const float* dqacc, void* dq, long long elems, float scale,
+                           long long acc_stride, int ways, int causal, int N, int S, int d, int grid,
                            cudaStream_t stream);
 }  // namespace dab
 
@@ -133,20 +134,23 @@ dab_status_t check_enums(dab_mask_t mask, dab_sched_t sched) {
   return DAB_OK;
 }
 
-bool layout(int B, int H, int S, int d, dab_ws_layout_t* L) {
+int acc_ways(dab_sched_t sched) { return sched == DAB_SCHED_ATOMIC ? 1 : dab::kAccWays; }
+
+bool layout(int B, int H, int S, int d, dab_sched_t sched, dab_ws_layout_t* L) {
   if (check_shape(B, H, S, d) != DAB_OK) return false;
   const size_t BH = (size_t)B * H, N = (size_t)S / 128, rows = BH * S;
+  const size_t ways = (size_t)acc_ways(sched);
   size_t off = 0;
   L->status = off;
   off += 256;
   L->sem = off;
-  off = round_up(off + BH * N * 8 * 4, 256);  // 8 semaphores per dQ tile
+  off = round_up(off + BH * N * dab::kSubTiles * ways * 4, 256);  // per tile, sub-tile, buffer
   L->D = off;
   off = round_up(off + rows * 4, 256);
   L->lse2 = off;
   off = round_up(off + rows * 4, 256);
   L->dqacc = off;
-  off = round_up(off + rows * (size_t)d * 4, 256);
+  off = round_up(off + ways * rows * (size_t)d * 4, 256);
   L->total = off;
   return true;
 }
@@ -180,7 +184,7 @@ const char* dab_status_string(dab_status_t s) {
 dab_status_t dab_bwd_workspace_layout(int B, int H, int S, int d, dab_mask_t mask, dab_sched_t sched,
                                       dab_ws_layout_t* L) {
   if (L == nullptr || check_enums(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
-  return layout(B, H, S, d, L) ? DAB_OK : DAB_ERR_INVALID_ARG;
+  return layout(B, H, S, d, sched, L) ? DAB_OK : DAB_ERR_INVALID_ARG;
 }
 
 size_t dab_bwd_workspace_size(int B, int H, int S, int d, dab_mask_t mask, dab_sched_t sched) {
@@ -230,14 +234,14 @@ dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dou
   if (check_shape(B, H, S, d) != DAB_OK || check_enums(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
   if (!aligned16(o) || !aligned16(lse) || !aligned16(dout)) return DAB_ERR_INVALID_ARG;
   dab_ws_layout_t L;
-  layout(B, H, S, d, &L);
+  layout(B, H, S, d, sched, &L);
   if (workspace == nullptr || !aligned16(workspace)) return DAB_ERR_WORKSPACE;
   if (ws_bytes < L.total) return DAB_ERR_WORKSPACE;
   int sms = 0;
   if (!device_setup(nullptr, &sms)) return DAB_ERR_UNSUPPORTED;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const long long rows = (long long)B * H * S;
-  const int n_sem = B * H * (S / 128) * 8;
+  const int n_sem = B * H * (S / 128) * dab::kSubTiles * acc_ways(sched);
   float* dqacc = (sched == DAB_SCHED_ATOMIC) ? reinterpret_cast<float*>(ws + L.dqacc) : nullptr;
   const int grid = elementwise_grid(sms, rows * (d / 8));
   cudaError_t e = dab::launch_preprocess(
@@ -260,7 +264,7 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
   const int N = S / 128;
   if (sched == DAB_SCHED_SHIFT && mask == DAB_MASK_CAUSAL && (N % 2) != 0) return DAB_ERR_UNSUPPORTED;
   dab_ws_layout_t L;
-  layout(B, H, S, d, &L);
+  layout(B, H, S, d, sched, &L);
   if (workspace == nullptr || !aligned16(workspace) || ws_bytes < L.total) return DAB_ERR_WORKSPACE;
   int sms = 0;
   if (!device_setup(nullptr, &sms)) return DAB_ERR_UNSUPPORTED;
@@ -292,6 +296,8 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
   p.lse2 = reinterpret_cast<const float*>(ws + L.lse2);
   p.D = reinterpret_cast<const float*>(ws + L.D);
   p.dqacc = reinterpret_cast<float*>(ws + L.dqacc);
+  p.acc_ways = acc_ways(sched);
+  p.acc_stride = rows * d;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.sem = reinterpret_cast<uint32_t*>(ws + L.sem);
@@ -325,7 +331,9 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
 
   if (!(flags & DAB_BWD_SKIP_CONVERT)) {
     const long long elems = rows * d;
-    e = dab::launch_convert(p.dqacc, dq, elems, scale, elementwise_grid(sms, elems / 4), stream);
+    e = dab::launch_convert(p.dqacc, dq, elems, scale, p.acc_stride, p.acc_ways,
+                            mask == DAB_MASK_CAUSAL ? 1 : 0, N, S, d, elementwise_grid(sms, elems / 4),
+                            stream);
     if (e != cudaSuccess) return cuda_fail(e, "convert launch");
   }
   return DAB_OK;

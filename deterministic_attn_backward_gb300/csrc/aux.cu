@@ -5,7 +5,8 @@
 //             recomputation, and the reset of everything the main kernel
 //             needs at zero (status word, dispatch counter, dQ semaphores;
 //             the f32 dQ accumulator too for the unordered atomic schedule).
-// convert:    dQ = bf16(scale * dQacc).
+// convert:    dQ = bf16(scale * (dQacc_0 + dQacc_1 + ...)), the accumulation
+//             buffers added in index order.
 // Both are grid-stride loops over 16-byte vectors, sized to a multiple of the
 // SM count by the host.
 #include <cuda_bf16.h>
@@ -81,14 +82,27 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
 
 __global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__ acc,
                                                       uint2* __restrict__ out, long long n_vec4,
-                                                      float scale) {
+                                                      float scale, long long acc_stride_vec4,
+                                                      int ways, int causal, int N, int S, int d) {
   const long long n = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec4; i += n) {
-    const float4 v = acc[i];
-    uint2 w;
-    w.x = pack_bf16x2(scale * v.x, scale * v.y);
-    w.y = pack_bf16x2(scale * v.z, scale * v.w);
-    out[i] = w;
+    // buffers that received a contribution: all of them, except for causal
+    // Q tiles with fewer contributors (tile j has j + 1)
+    int nacc = ways;
+    if (causal && ways > 1) {
+      const long long row = (i * 4) / d;
+      const int j = (int)((row % S) / kTile);
+      if (j + 1 < nacc) nacc = j + 1;
+    }
+    float4 v = acc[i];
+    for (int m = 1; m < nacc; ++m) {  // fixed order: buffer 0, 1, ...
+      const float4 w = acc[i + (long long)m * acc_stride_vec4];
+      v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+    }
+    uint2 o;
+    o.x = pack_bf16x2(scale * v.x, scale * v.y);
+    o.y = pack_bf16x2(scale * v.z, scale * v.w);
+    out[i] = o;
   }
 }
 
@@ -111,10 +125,12 @@ cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const flo
   return cudaGetLastError();
 }
 
-cudaError_t launch_convert(const float* dqacc, void* dq, long long elems, float scale, int grid,
+cudaError_t launch_convert(const float* dqacc, void* dq, long long elems, float scale,
+                           long long acc_stride, int ways, int causal, int N, int S, int d, int grid,
                            cudaStream_t stream) {
   convert_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dqacc),
-                                           reinterpret_cast<uint2*>(dq), elems / 4, scale);
+                                           reinterpret_cast<uint2*>(dq), elems / 4, scale,
+                                           acc_stride / 4, ways, causal, N, S, d);
   return cudaGetLastError();
 }
 

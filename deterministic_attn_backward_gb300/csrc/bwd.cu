@@ -43,7 +43,6 @@ namespace {
 constexpr int kThreads = 640;
 constexpr int kSoftmaxWarp0 = 4;    // warps 4-7: Q columns 0-63, warps 8-11: 64-127
 constexpr int kReducerWarp0 = 12;   // warps 12-19: two reducer warpgroups
-constexpr int kSubTiles = 8;        // dQ tile = 8 sub-tiles, one semaphore and reducer warp each
 
 template <int HD>
 struct Cfg {
@@ -488,9 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     // eighth of the tile into the f32 accumulator:
     //   d = 128 (dQ^T, lanes = d):  d columns 32*quad.., Q rows 64*half..+63
     //   d =  64 (dQ, lanes = Q rows): Q rows 32*quad.., d columns 32*half..+31
-    // For the ordered schedules every eighth has its own semaphore, so
-    // consecutive contributors to one dQ tile overlap on different eighths
-    // while each element still receives its partial sums in rank order.
+    // For the ordered schedules every eighth of every accumulation buffer has
+    // its own semaphore, so consecutive contributors to one dQ tile overlap
+    // on different eighths and buffers while each element of a buffer still
+    // receives its partial sums in rank order.
     const int quad = warp & 3;                          // tensor-memory lane quadrant
     const int half = (warp - kReducerWarp0) >> 2;
     const int sub = half * 4 + quad;                    // sub-tile / semaphore index
@@ -512,13 +512,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       for (int t = 0; t < steps; ++t) {
         const Step st = step(p.sched, p.mask, p.N, u, t);
         // everything but the values is computed before the drain
+        // rank r -> buffer r mod ways, position r / ways within that buffer
         const int rank = deterministic ? dab::rank(p.sched, p.mask, p.N, st.kv, st.q) : 0;
-        uint32_t* sem = p.sem + ((size_t)bh * p.N + st.q) * kSubTiles + sub;
-        const uint32_t sem_detail = (uint32_t)((bh * p.N + st.q) * kSubTiles + sub);
-        const bool store = deterministic && rank == 0;  // the first contribution overwrites
+        const int way = rank % p.acc_ways, lrank = rank / p.acc_ways;
+        const size_t sem_idx = (((size_t)bh * p.N + st.q) * kSubTiles + sub) * p.acc_ways + way;
+        uint32_t* sem = p.sem + sem_idx;
+        const uint32_t sem_detail = (uint32_t)sem_idx;
+        const bool store = deterministic && lrank == 0;  // a buffer's first contribution overwrites
         const size_t row0 = (size_t)bh * p.S + (size_t)st.q * kTile;
-        float* base = (HD == 128) ? p.dqacc + (row0 + (size_t)half * 64) * HD + r
-                                  : p.dqacc + (row0 + (size_t)r) * HD + half * 32;
+        float* acc = p.dqacc + (size_t)way * (size_t)p.acc_stride;
+        float* base = (HD == 128) ? acc + (row0 + (size_t)half * 64) * HD + r
+                                  : acc + (row0 + (size_t)r) * HD + half * 32;
         if (!warp_wait(&bars->dq_full, s & 1, wc, 41)) { ok = false; break; }
         tc_fence_after();
         uint32_t v[kVals];
@@ -531,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         if (lane == 0) mbar_arrive(&bars->dq_empty);
         if (deterministic) {
           int g = 1;
-          if (lane == 0) g = sem_wait(sem, (uint32_t)rank, wc, sem_detail) ? 1 : 0;
+          if (lane == 0) g = sem_wait(sem, (uint32_t)lrank, wc, sem_detail) ? 1 : 0;
           g = __shfl_sync(0xffffffffu, g, 0);
           if (!g) { ok = false; break; }
         }
@@ -541,7 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             for (int q = 0; q < 64; ++q) base[(size_t)q * HD] = __uint_as_float(v[q]);
           } else {
 #pragma unroll
-            for (int q = 0; q < 64; ++q) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
+            for (int q = 0; q < 64; ++q) {
+              red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
+              // Ordered schedules: spread the adds out so that they do not
+              // fill the SM's memory-instruction queue in one burst (the
+              // softmax warps' shared-memory loads wait behind them).
+              if (deterministic && (q & 7) == 7) __nanosleep(20);
+            }
           }
         } else {
 #pragma unroll
@@ -559,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           // rank + 1 (fence per lane, warp barrier, lane 0's release store).
           fence_acq_rel_gpu();
           __syncwarp();
-          if (lane == 0) st_release_gpu(sem, (uint32_t)rank + 1u);
+          if (lane == 0) st_release_gpu(sem, (uint32_t)lrank + 1u);
         }
         ++s;
       }

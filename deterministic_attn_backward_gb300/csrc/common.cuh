@@ -32,11 +32,21 @@ enum : uint32_t {
 
 constexpr int kTile = 128;  // rows of a KV tile and of a Q tile
 
+// The ordered schedules accumulate dQ in kAccWays interleaved f32 buffers:
+// the partial of rank r goes to buffer r mod kAccWays, in rank order within
+// the buffer, and the convert kernel adds the buffers in index order.  A
+// contributor then waits for rank r - kAccWays instead of r - 1, which hides
+// the latency of the cross-SM hand-off; the summation order stays fixed.
+constexpr int kAccWays = 2;
+constexpr int kSubTiles = 8;  // semaphores (and reducer warps) per dQ tile per buffer
+
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [B*H*S, d] bf16, box 64 x 128, 128B swizzle
   const float* lse2;                    // [B*H*S] LSE * log2(e)
   const float* D;                       // [B*H*S]
-  float* dqacc;                         // [B*H*S, d] f32
+  float* dqacc;                         // [acc_ways][B*H*S, d] f32
+  long long acc_stride;                 // floats between two accumulation buffers
+  int acc_ways;                         // kAccWays (ordered schedules) or 1 (atomic)
   __nv_bfloat16* dk;                    // [B*H*S, d]
   __nv_bfloat16* dv;
   uint32_t* sem;                        // [B*H, N]

@@ -96,8 +96,10 @@ dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v,
 
 /* Bytes of device workspace that dab_attn_bwd needs for this problem (0 on
  * invalid arguments).  The workspace holds the status word, the dispatch
- * counter, eight semaphores per 128-row dQ tile (one per eighth), D and
- * LSE*log2(e) per row, and the float32 dQ accumulator [B][H][S][d].  It needs no initialisation: the
+ * counter, the semaphores (per 128-row dQ tile: one per eighth of the tile
+ * and per accumulation buffer), D and LSE*log2(e) per row, and the float32
+ * dQ accumulation buffers [ways][B][H][S][d] (two interleaved buffers for
+ * the ordered schedules, one for ATOMIC).  It needs no initialisation: the
  * first kernel of every backward call resets what must start at zero.      */
 size_t dab_bwd_workspace_size(int B, int H, int S, int d,
                               dab_mask_t mask, dab_sched_t sched);
@@ -112,7 +114,8 @@ size_t dab_bwd_workspace_size(int B, int H, int S, int d,
  *      dQ partial on the tensor cores, then the dQ reduction in the order
  *      `sched` defines (semaphore-ordered, no float atomics, for the three
  *      deterministic schedules);
- *   3. the convert kernel: dQ = bf16(scale * dQacc).
+ *   3. the convert kernel: dQ = bf16(scale * sum of the accumulation
+ *      buffers, added in buffer order).
  * The call returns once the kernels are queued.                              */
 dab_status_t dab_attn_bwd(const void* q, const void* k, const void* v,
                           const void* o, const float* lse, const void* dout,
@@ -170,10 +173,10 @@ dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dou
 /* Byte offsets of the workspace regions (for tests and tools).             */
 typedef struct {
     size_t status;   /* uint32 status word, uint32 error detail, uint32 counter */
-    size_t sem;      /* uint32 [B*H][N][8] semaphores (one per dQ-tile eighth)   */
+    size_t sem;      /* uint32 [B*H][N][8][ways] semaphores                     */
     size_t D;        /* float  [B*H*S]                                          */
     size_t lse2;     /* float  [B*H*S] LSE * log2(e)                            */
-    size_t dqacc;    /* float  [B*H*S][d]                                       */
+    size_t dqacc;    /* float  [ways][B*H*S][d]                                 */
     size_t total;
 } dab_ws_layout_t;
 
@@ -196,7 +199,8 @@ dab_status_t dab_bwd_workspace_layout(int B, int H, int S, int d,
  *
  *   Limit    problems whose dab_bwd_workspace_size() exceeds
  *            DAB_NOALLOC_SCRATCH_BYTES are rejected with DAB_ERR_WORKSPACE
- *            before anything is launched (roughly B*H*S*d <= 8M elements).
+ *            before anything is launched (roughly B*H*S*d <= 4M elements
+ *            for the ordered schedules, 8M for ATOMIC).
  *   Set-up   the first call on a device, with that device current, looks up
  *            the array's device address (cudaGetSymbolAddress) and caches
  *            it; make that first call before any stream capture.  A failed

@@ -49,12 +49,15 @@ def test_workspace_layout(lib):
     L = dab.workspace_layout(B, H, S, d, "causal", "descending_q")
     rows = B * H * S
     assert L.status == 0 and L.sem == 256
-    assert L.D >= L.sem + 32 * B * H * (S // 128)
+    ways = 2  # ordered schedules: two interleaved accumulation buffers
+    assert L.D >= L.sem + 4 * 8 * ways * B * H * (S // 128)
     assert L.lse2 >= L.D + 4 * rows and L.dqacc >= L.lse2 + 4 * rows
-    assert L.total >= L.dqacc + 4 * rows * d
+    assert L.total >= L.dqacc + ways * 4 * rows * d
+    La = dab.workspace_layout(B, H, S, d, "causal", "atomic")  # one buffer
+    assert La.total >= La.dqacc + 4 * rows * d and La.total < L.total
     for off in (L.sem, L.D, L.lse2, L.dqacc, L.total):
         assert off % 256 == 0
-    assert dab.workspace_size(B, H, S, d) == L.total
+    assert dab.workspace_size(B, H, S, d, "causal", "descending_q") == L.total
     assert lib.dab_bwd_workspace_size(B, H, 100, d, 0, 0) == 0      # S not a multiple of 128
     assert lib.dab_bwd_workspace_size(B, H, S, 96, 0, 0) == 0       # d not 64/128
     assert lib.dab_bwd_workspace_size(B, H, S, d, 2, 0) == 0        # bad mask
