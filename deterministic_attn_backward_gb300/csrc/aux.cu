@@ -86,10 +86,10 @@ __global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__
                                                       int ways, int causal, int N, int S, int d) {
   const long long n = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec4; i += n) {
-    // buffers that received a contribution: all of them, except for causal
-    // Q tiles with fewer contributors (tile j has j + 1)
-    int nacc = ways;
-    if (causal && ways > 1) {
+    // buffers that received a contribution: min(ways, contributors of the Q
+    // tile), with N contributors per tile for the full mask, j + 1 for causal
+    int nacc = ways < N ? ways : N;
+    if (causal && nacc > 1) {
       const long long row = (i * 4) / d;
       const int j = (int)((row % S) / kTile);
       if (j + 1 < nacc) nacc = j + 1;
