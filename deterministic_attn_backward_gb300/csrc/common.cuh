@@ -37,7 +37,7 @@ constexpr int kTile = 128;  // rows of a KV tile and of a Q tile
 // the buffer, and the convert kernel adds the buffers in index order.  A
 // contributor then waits for rank r - kAccWays instead of r - 1, which hides
 // the latency of the cross-SM hand-off; the summation order stays fixed.
-constexpr int kAccWays = 2;
+constexpr int kAccWays = 4;
 constexpr int kSubTiles = 8;  // semaphores (and reducer warps) per dQ tile per buffer
 
 struct BwdParams {

@@ -98,7 +98,7 @@ dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v,
  * invalid arguments).  The workspace holds the status word, the dispatch
  * counter, the semaphores (per 128-row dQ tile: one per eighth of the tile
  * and per accumulation buffer), D and LSE*log2(e) per row, and the float32
- * dQ accumulation buffers [ways][B][H][S][d] (two interleaved buffers for
+ * dQ accumulation buffers [ways][B][H][S][d] (four interleaved buffers for
  * the ordered schedules, one for ATOMIC).  It needs no initialisation: the
  * first kernel of every backward call resets what must start at zero.      */
 size_t dab_bwd_workspace_size(int B, int H, int S, int d,
@@ -199,7 +199,7 @@ dab_status_t dab_bwd_workspace_layout(int B, int H, int S, int d,
  *
  *   Limit    problems whose dab_bwd_workspace_size() exceeds
  *            DAB_NOALLOC_SCRATCH_BYTES are rejected with DAB_ERR_WORKSPACE
- *            before anything is launched (roughly B*H*S*d <= 4M elements
+ *            before anything is launched (roughly B*H*S*d <= 2M elements
  *            for the ordered schedules, 8M for ATOMIC).
  *   Set-up   the first call on a device, with that device current, looks up
  *            the array's device address (cudaGetSymbolAddress) and caches

@@ -49,7 +49,7 @@ def test_workspace_layout(lib):
     L = dab.workspace_layout(B, H, S, d, "causal", "descending_q")
     rows = B * H * S
     assert L.status == 0 and L.sem == 256
-    ways = 2  # ordered schedules: two interleaved accumulation buffers
+    ways = 4  # ordered schedules: four interleaved accumulation buffers
     assert L.D >= L.sem + 4 * 8 * ways * B * H * (S // 128)
     assert L.lse2 >= L.D + 4 * rows and L.dqacc >= L.lse2 + 4 * rows
     assert L.total >= L.dqacc + ways * 4 * rows * d

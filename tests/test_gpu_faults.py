@@ -20,8 +20,8 @@ def test_poisoned_semaphore_times_out(sched):
     ws = dab.new_workspace(B, H, S, d, mask, sched)
     L = dab.workspace_layout(B, H, S, d, mask, sched)
     dab.bwd_preprocess(o, lse, do, mask, sched, ws)
-    sem = ws[L.sem:L.D].view(torch.int32)  # [head][Q tile][8 sub-tiles][2 buffers]
-    sem[16:32] = 1000  # every semaphore of Q tile 1 of head 0: nobody waits for 1000
+    sem = ws[L.sem:L.D].view(torch.int32)  # [head][Q tile][8 sub-tiles][4 buffers]
+    sem[32:64] = 1000  # every semaphore of Q tile 1 of head 0: nobody waits for 1000
     opts = dab.BwdOpts(spin_timeout_ns=50_000_000, flags=dab.DAB_BWD_SKIP_PREPROCESS, grid=0)
     dab.attn_bwd(q, k, v, o, lse, do, mask, sched, workspace=ws, opts=opts)
     assert dab.check_status(ws) == 5  # DAB_ERR_TIMEOUT
