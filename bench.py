@@ -160,7 +160,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     q, k, v, do = inputs.make_qkvdo(B, H, S, D, SEED, QK_SCALE)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     fwd = {m: dab.attn_fwd(qd, kd, vd, m) for m in MASKS}
-    ws = {m: dab.new_workspace(B, H, S, D, m, "atomic", dev) for m in MASKS}
+    ws = {m: dab.new_workspace(B, H, S, D, m, "serial", dev) for m in MASKS}  # largest (ordered)
     outs = {m: tuple(torch.empty_like(qd) for _ in range(3)) for m in MASKS}
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
