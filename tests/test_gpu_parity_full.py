@@ -1,0 +1,87 @@
+"""CUDA backward against the float64 oracle at the full workload sizes.
+
+The whole backward runs on the GPU at the benchmark's sizes and launch
+configuration; the oracle recomputes, exactly, sampled outputs: 64 query rows
+(O, LSE, dQ) and 64 key rows (dK, dV) of sampled heads, spread over the first,
+middle and last tiles.  Key rows need the LSE and D of every query row of
+their head, so each sampled head costs one whole-head pass of the oracle.
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import deterministic_attn_backward_gb300 as dab
+from deterministic_attn_backward_gb300 import inputs
+from gpu_common import TOL
+
+# (name, B, H, S, d, seed, qk_scale, masks, schedules, sampled heads)
+CONFIGS = [
+    ("b4h16s2048d64", 4, 16, 2048, 64, 1, 1.0, ("full",),
+     ("serial", "descending_q", "shift", "atomic"), ((0, 0), (3, 15))),
+    ("b2h16s8192d128", 2, 16, 8192, 128, 2, 0.5, ("causal", "full"),
+     ("serial", "descending_q", "shift", "atomic"), ((0, 0), (1, 15))),
+    ("b1h32s16384d128", 1, 32, 16384, 128, 3, 1.0, ("full", "causal"),
+     ("descending_q", "shift", "atomic"), ((0, 31),)),
+    ("b1h16s32768d128", 1, 16, 32768, 128, 4, 1.0, ("causal", "full"),
+     ("descending_q", "shift"), ((0, 7),)),
+]
+
+
+def _rows(S):
+    picks = [0, 1, 127, 128, S // 2 - 1, S // 2, S - 129, S - 128, S - 2, S - 1]
+    rng = np.random.default_rng(S)
+    picks += list(rng.choice(S, 64 - len(picks), replace=False))
+    return sorted(set(int(x) for x in picks))[:64]
+
+
+@functools.lru_cache(maxsize=4)
+def _inputs(B, H, S, d, seed, qks):
+    return inputs.make_qkvdo(B, H, S, d, seed, qks)
+
+
+@functools.lru_cache(maxsize=16)
+def _reference(B, H, S, d, seed, qks, mask, b, h):
+    q, k, v, do = _inputs(B, H, S, d, seed, qks)
+    rows = _rows(S)
+    return rows, oracle.attn_rows(q[b, h], k[b, h], v[b, h], do[b, h], d ** -0.5,
+                                  mask == "causal", rows, rows)
+
+
+def _err(got, want):
+    return float(np.max(np.abs(got - want)) / max(np.max(np.abs(want)), 1e-30))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cfg", CONFIGS, ids=[c[0] for c in CONFIGS])
+def test_full_size_sampled_parity(cfg):
+    name, B, H, S, d, seed, qks, masks, scheds, heads = cfg
+    q, k, v, do = _inputs(B, H, S, d, seed, qks)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    ws = dab.new_workspace(B, H, S, d, "full", "serial")  # the largest workspace
+    for mask in masks:
+        o, lse = dab.attn_fwd(qd, kd, vd, mask)
+        grads = {}
+        for sched in scheds:
+            dq, dk, dv = dab.attn_bwd(qd, kd, vd, o, lse, dod, mask, sched, workspace=ws)
+            assert dab.check_status(ws) == 0, (mask, sched)
+            grads[sched] = (dq, dk, dv)
+        for b, h in heads:
+            rows, ref = _reference(B, H, S, d, seed, qks, mask, b, h)
+            idx = torch.tensor(rows, device="cuda")
+            got_o = o[b, h].index_select(0, idx).double().cpu().numpy()
+            got_lse = lse[b, h].index_select(0, idx).double().cpu().numpy()
+            assert _err(got_o, ref["o"]) < TOL, (mask, "o")
+            assert np.max(np.abs(got_lse - ref["lse"])) < 1e-3, (mask, "lse")
+            for sched, (dq, dk, dv) in grads.items():
+                for nm, t, want in (("dq", dq, ref["dq"]), ("dk", dk, ref["dk"]),
+                                    ("dv", dv, ref["dv"])):
+                    got = t[b, h].index_select(0, idx).double().cpu().numpy()
+                    e = _err(got, want)
+                    assert e < TOL, f"{name} {mask} {sched} {nm}: {e:.3e}"
+        if "serial" in grads and "descending_q" in grads:
+            # same dQ reduction order: same dQ bits
+            assert torch.equal(grads["serial"][0].view(torch.int16),
+                               grads["descending_q"][0].view(torch.int16))
