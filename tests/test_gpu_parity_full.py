@@ -1,10 +1,13 @@
 """CUDA backward against the float64 oracle at the full workload sizes.
 
 The whole backward runs on the GPU at the benchmark's sizes and launch
-configuration; the oracle recomputes, exactly, sampled outputs: 64 query rows
-(O, LSE, dQ) and 64 key rows (dK, dV) of sampled heads, spread over the first,
-middle and last tiles.  Key rows need the LSE and D of every query row of
-their head, so each sampled head costs one whole-head pass of the oracle.
+configuration; the oracle recomputes, in float64, every output of one or two
+sampled heads (O, LSE, dQ, dK, dV), and each gradient of a sampled head is
+compared over the whole head with max|gpu - ref| / max|ref| <= 1e-2.  The
+denominator is the head's own maximum: in a causal head the largest gradients
+sit in the first few query rows (few keys, large softmax weights), so a
+denominator taken over a subset of rows would judge the rest against a
+smaller scale than the tensor's.
 """
 import functools
 
@@ -30,13 +33,6 @@ CONFIGS = [
 ]
 
 
-def _rows(S):
-    picks = [0, 1, 127, 128, S // 2 - 1, S // 2, S - 129, S - 128, S - 2, S - 1]
-    rng = np.random.default_rng(S)
-    picks += list(rng.choice(S, 64 - len(picks), replace=False))
-    return sorted(set(int(x) for x in picks))[:64]
-
-
 @functools.lru_cache(maxsize=4)
 def _inputs(B, H, S, d, seed, qks):
     return inputs.make_qkvdo(B, H, S, d, seed, qks)
@@ -45,9 +41,8 @@ def _inputs(B, H, S, d, seed, qks):
 @functools.lru_cache(maxsize=16)
 def _reference(B, H, S, d, seed, qks, mask, b, h):
     q, k, v, do = _inputs(B, H, S, d, seed, qks)
-    rows = _rows(S)
-    return rows, oracle.attn_rows(q[b, h], k[b, h], v[b, h], do[b, h], d ** -0.5,
-                                  mask == "causal", rows, rows)
+    return oracle.attn_fwd_bwd(q[b, h], k[b, h], v[b, h], do[b, h], d ** -0.5,
+                               mask == "causal")
 
 
 def _err(got, want):
@@ -69,17 +64,13 @@ def test_full_size_sampled_parity(cfg):
             assert dab.check_status(ws) == 0, (mask, sched)
             grads[sched] = (dq, dk, dv)
         for b, h in heads:
-            rows, ref = _reference(B, H, S, d, seed, qks, mask, b, h)
-            idx = torch.tensor(rows, device="cuda")
-            got_o = o[b, h].index_select(0, idx).double().cpu().numpy()
-            got_lse = lse[b, h].index_select(0, idx).double().cpu().numpy()
-            assert _err(got_o, ref["o"]) < TOL, (mask, "o")
-            assert np.max(np.abs(got_lse - ref["lse"])) < 1e-3, (mask, "lse")
+            ref = _reference(B, H, S, d, seed, qks, mask, b, h)
+            assert _err(o[b, h].double().cpu().numpy(), ref["o"]) < TOL, (mask, "o")
+            assert np.max(np.abs(lse[b, h].double().cpu().numpy() - ref["lse"])) < 1e-3
             for sched, (dq, dk, dv) in grads.items():
-                for nm, t, want in (("dq", dq, ref["dq"]), ("dk", dk, ref["dk"]),
-                                    ("dv", dv, ref["dv"])):
-                    got = t[b, h].index_select(0, idx).double().cpu().numpy()
-                    e = _err(got, want)
+                for nm, t, want in (("dq", dq[b, h], ref["dq"]), ("dk", dk[b, h], ref["dk"]),
+                                    ("dv", dv[b, h], ref["dv"])):
+                    e = _err(t.double().cpu().numpy(), want)
                     assert e < TOL, f"{name} {mask} {sched} {nm}: {e:.3e}"
         if "serial" in grads and "descending_q" in grads:
             # same dQ reduction order: same dQ bits
