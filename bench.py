@@ -39,8 +39,8 @@ DET_SCHEDS = ("serial", "descending_q", "shift")
 # number of heads, so x2), keyed by the SHA-1 of the kernel source it was
 # taken on.  Reported only while the source is unchanged.
 TRAFFIC_CAPTURES = {
-    # causal 137.2 + 277.8 MB, full 140.0 + 296.7 MB: mean of the masks, x2
-    "2aa60cf5aff8b1246459624cd9b50baaf79449b7": 2 * ((137.209856 + 277.820672) + (140.017408 + 296.656384)) / 2 * 1e6,
+    # causal 136.7 + 276.4 MB, full 138.6 + 294.0 MB: mean of the masks, x2
+    "47b61baf0fa4537fe9081a3c62c2a0eca14d8a61": 2 * ((136.651520 + 276.430592) + (138.601216 + 293.974528)) / 2 * 1e6,
 }
 MASKS = ("causal", "full")
 
@@ -236,6 +236,13 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         main_ms[m] = tot / reps
     check()
 
+    # ---- side kernels alone (HBM-bound): preprocess, and convert with the main
+    # kernel skipped, on the causal workspace of the step's schedule
+    side = side_kernels(dab, qd, kd, vd, dod, fwd["causal"], "causal", step_scheds["causal"],
+                        ws["causal"], outs["causal"], stream, ev)
+    own_peak = dab.mma_peak(iters=20000)
+    check()
+
     # ---- the timed region
     for _ in range(args.warmup):
         step()
@@ -309,6 +316,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                      "traffic": traffic_for_current_kernel(),
                      "kernel": "bwd_kernel<128>", "peak_source": peaks["source"] + " (burst)",
                      "launch_ms": {m: round(x, 4) for m, x in main_ms.items()}},
+        "own_tensor_peak": {"tflops": round(own_peak["tflops"], 1),
+                            "frac": round(achieved / own_peak["tflops"], 4),
+                            "how": "dab_mma_peak: one CTA per SM, back-to-back tcgen05.mma "
+                                   "128x256x16 from shared memory"},
+        "side_kernels": side,
         "per_schedule": per,
         "e2e": {"value": round(world * step_flops / (e2e_ms * 1e9), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -317,6 +329,103 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         "clocks": clocks,
         "cpu_baseline": cpu_baseline(),
     }
+
+
+def side_kernels(dab, qd, kd, vd, dod, fwd_m, mask, sched, ws, out, stream, ev, reps=10) -> dict:
+    """Preprocess and convert timed alone (CUDA events, median of `reps`), with
+    their algorithmic bytes: preprocess reads O, dO, LSE and writes D and
+    LSE*log2(e); convert reads one f32 accumulator and writes bf16 dQ (the
+    minimum), and `actual_bytes` counts the accumulation buffers it really
+    reads (four for the ordered schedules)."""
+    o, lse = fwd_m
+    Bq, Hq, Sq, Dq = qd.shape
+    rows, elems = Bq * Hq * Sq, Bq * Hq * Sq * Dq
+    peaks = load_peaks()
+
+    def timed(fn):
+        ts = []
+        for it in range(reps + 3):
+            a, b_ = ev(), ev()
+            a.record(stream)
+            fn()
+            b_.record(stream)
+            b_.synchronize()
+            if it >= 3:
+                ts.append(a.elapsed_time(b_))
+        return statistics.median(ts)
+
+    pre_ms = timed(lambda: dab.bwd_preprocess(o, lse, dod, mask, sched, ws))
+    conv_opts = dab.BwdOpts(spin_timeout_ns=0,
+                            flags=dab.DAB_BWD_SKIP_PREPROCESS | dab.DAB_BWD_SKIP_MAIN, grid=0)
+    conv_ms = timed(lambda: dab.attn_bwd(qd, kd, vd, o, lse, dod, mask, sched, workspace=ws,
+                                         out=out, opts=conv_opts))
+    ways = 1 if sched == "atomic" else 4
+    pre_b = 4 * elems + 12 * rows
+    conv_b, conv_actual = 6 * elems, (4 * ways + 2) * elems
+    gbs = lambda b, ms: round(b / (ms * 1e-3) / 1e9, 1)
+    hbm = peaks["hbm_gbs"]
+    return {"preprocess": {"ms": round(pre_ms, 4), "bytes": pre_b, "gbs": gbs(pre_b, pre_ms),
+                           "frac": round(pre_b / (pre_ms * 1e-3) / 1e9 / hbm, 3)},
+            "convert": {"ms": round(conv_ms, 4), "bytes": conv_b, "gbs": gbs(conv_b, conv_ms),
+                        "actual_bytes": conv_actual, "actual_gbs": gbs(conv_actual, conv_ms),
+                        "frac_actual": round(conv_actual / (conv_ms * 1e-3) / 1e9 / hbm, 3)},
+            "peak_gbs": hbm, "peak_source": peaks["source"]}
+
+
+# Measurement configurations: (name, B, H, S, d, seed, qk scale, masks).
+SWEEP_CONFIGS = [
+    ("C1", 4, 16, 2048, 64, 1, 1.0, ("full",)),
+    ("C2", 2, 16, 8192, 128, 2, 0.5, ("causal", "full")),
+    ("C3", 1, 32, 16384, 128, 3, 1.0, ("full", "causal")),
+] + [(f"C4-s{s_}-d{d_}", 32768 // s_, 16, s_, d_, 4, 1.0, ("full", "causal"))
+     for d_ in (64, 128) for s_ in (1024, 2048, 4096, 8192, 16384, 32768)]
+
+
+def run_sweep(which: str, reps: int) -> None:
+    """Every schedule on every measurement configuration: per (config, mask)
+    one JSON line with ms, TFLOP/s, fraction of the measured peak and the gap
+    closure (T_serial - T_sched) / (T_serial - T_atomic); medians of `reps`
+    timed calls after three warm-up calls."""
+    import torch
+    import deterministic_attn_backward_gb300 as dab
+    from deterministic_attn_backward_gb300 import inputs
+    dab.load_library()
+    peak = load_peaks()["bf16_tflops"]
+    stream = torch.cuda.current_stream()
+    for name, b, h, s_, d, seed, qks, masks in SWEEP_CONFIGS:
+        if which != "all" and not name.startswith(which):
+            continue
+        q, k, v, do = (t.cuda() for t in inputs.make_qkvdo(b, h, s_, d, seed, qks))
+        ws = dab.new_workspace(b, h, s_, d, "full", "serial")
+        out = tuple(torch.empty_like(q) for _ in range(3))
+        for mask in masks:
+            o, lse = dab.attn_fwd(q, k, v, mask)
+            fl = 10.0 * b * h * s_ * s_ * d * (1.0 if mask == "full" else 0.5)
+            row = {"config": name, "B": b, "H": h, "S": s_, "d": d, "mask": mask, "scheds": {}}
+            for sched in ALL_SCHEDS:
+                ts = []
+                for it in range(3 + reps):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    dab.attn_bwd(q, k, v, o, lse, do, mask, sched, workspace=ws, out=out)
+                    e1.record(stream)
+                    e1.synchronize()
+                    if it >= 3:
+                        ts.append(e0.elapsed_time(e1))
+                st = dab.check_status(ws)
+                ms = statistics.median(ts)
+                tf = fl / (ms * 1e-3) / 1e12
+                row["scheds"][sched] = {"ms": round(ms, 4), "tflops": round(tf, 1),
+                                        "frac": round(tf / peak, 4), "status": st}
+            sc = row["scheds"]
+            gap = sc["serial"]["ms"] - sc["atomic"]["ms"]
+            for sched in ("descending_q", "shift"):
+                sc[sched]["gap_closure"] = (round((sc["serial"]["ms"] - sc[sched]["ms"]) / gap, 3)
+                                            if abs(gap) > 1e-9 else None)
+            print(json.dumps(row), flush=True)
+        del q, k, v, do, ws, out
+        torch.cuda.empty_cache()
 
 
 # ---------------------------------------------------------------- oracle
@@ -432,7 +541,12 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--case", default=None, help="B,H,S,d,mask,sched: time one configuration")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--sweep", default=None,
+                    help="all | C1 | C2 | C3 | C4: every schedule on the measurement configurations")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args.sweep, max(args.reps, 5))
+        return
     if args.case:
         for spec in args.case.split(";"):
             print(json.dumps(run_case(spec, args.reps)), flush=True)

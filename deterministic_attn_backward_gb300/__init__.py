@@ -24,13 +24,15 @@ STATUS = {0: "DAB_OK", 1: "DAB_ERR_INVALID_ARG", 2: "DAB_ERR_UNSUPPORTED", 3: "D
           4: "DAB_ERR_CUDA", 5: "DAB_ERR_TIMEOUT", 6: "DAB_ERR_DEVICE_BOUNDS"}
 DAB_BWD_SKIP_PREPROCESS = 0x1
 DAB_BWD_SKIP_CONVERT = 0x2
+DAB_BWD_SKIP_MAIN = 0x4
 
 EXPORTED = (
     "dab_attn_fwd", "dab_bwd_workspace_size", "dab_attn_bwd", "dab_check_status",
     "dab_status_string", "dab_attn_bwd_ex", "dab_bwd_preprocess", "dab_bwd_workspace_layout",
     "dab_sched_units_per_head", "dab_sched_unit_steps", "dab_sched_step", "dab_sched_rank",
     "dab_sched_contributors", "dab_sched_gang_size", "dab_dag_simulate", "dab_dag_critical_path",
-    "dab_selftest_mma", "dab_last_error_string", "dab_attn_bwd_noalloc",
+    "dab_selftest_mma", "dab_last_error_string", "dab_attn_bwd_noalloc", "dab_mma_peak",
+    "dab_mma_peak_grid",
 )
 
 
@@ -105,6 +107,10 @@ def load_library(path: str = LIB_PATH):
     lib.dab_attn_bwd_noalloc.restype = i
     lib.dab_selftest_mma.argtypes = [i] + [vp] * 10
     lib.dab_selftest_mma.restype = i
+    lib.dab_mma_peak.argtypes = [i, vp, vp]
+    lib.dab_mma_peak.restype = i
+    lib.dab_mma_peak_grid.argtypes = []
+    lib.dab_mma_peak_grid.restype = i
     _lib = lib
     return lib
 
@@ -278,3 +284,24 @@ def selftest_mma(d: int, x, y, z, pm):
                                 ws.data_ptr(), _stream(dev)), "dab_selftest_mma")
     _check(check_status(ws), "selftest device status")
     return out0, out1, out2, out3
+
+
+def mma_peak(iters: int = 100000, device=None) -> dict:
+    """Dense bf16 tensor throughput of the library's own tcgen05 path: one
+    timed launch of `iters` x 4 MMAs (128 x 256 x 16) per SM, after one
+    untimed warm-up launch.  Returns {"tflops", "ms", "grid", "iters"}."""
+    lib = load_library()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    stream = _stream(dev)
+    grid = lib.dab_mma_peak_grid()
+    _check(lib.dab_mma_peak(max(1, iters // 10), ws.data_ptr(), stream), "dab_mma_peak")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    _check(lib.dab_mma_peak(iters, ws.data_ptr(), stream), "dab_mma_peak")
+    e1.record()
+    e1.synchronize()
+    _check(check_status(ws), "dab_mma_peak device status")
+    ms = e0.elapsed_time(e1)
+    flops = float(grid) * iters * 4 * 2 * 128 * 256 * 16
+    return {"tflops": flops / (ms * 1e-3) / 1e12, "ms": ms, "grid": grid, "iters": iters}

@@ -23,6 +23,9 @@ template <int HD> int fwd_smem_bytes();
 template <int HD> const void* fwd_kernel_ptr();
 template <int HD> int selftest_smem_bytes();
 template <int HD> const void* selftest_kernel_ptr();
+int peak_smem_bytes();
+const void* peak_kernel_ptr();
+int peak_threads();
 cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const float* lse, float* D,
                               float* lse2, uint32_t* sem, int n_sem, WsHeader* hdr, float* dqacc,
                               long long dq_elems, int rows, int grid, cudaStream_t stream);
@@ -78,6 +81,9 @@ bool device_setup(int* dev_out, int* sms_out) {
       ok &= cudaFuncSetAttribute(dab::selftest_kernel_ptr<64>(),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  dab::selftest_smem_bytes<64>()) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(dab::peak_kernel_ptr(),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 dab::peak_smem_bytes()) == cudaSuccess;
       ok &= cudaFuncSetAttribute(dab::selftest_kernel_ptr<128>(),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  dab::selftest_smem_bytes<128>()) == cudaSuccess;
@@ -325,9 +331,11 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {&p};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, d == 128 ? dab::bwd_kernel_ptr<128>() : dab::bwd_kernel_ptr<64>(),
-                                      args);
-  if (e != cudaSuccess) return cuda_fail(e, "main kernel launch");
+  cudaError_t e = cudaSuccess;
+  if (!(flags & DAB_BWD_SKIP_MAIN)) {
+    e = cudaLaunchKernelExC(&cfg, d == 128 ? dab::bwd_kernel_ptr<128>() : dab::bwd_kernel_ptr<64>(), args);
+    if (e != cudaSuccess) return cuda_fail(e, "main kernel launch");
+  }
 
   if (!(flags & DAB_BWD_SKIP_CONVERT)) {
     const long long elems = rows * d;
@@ -418,6 +426,28 @@ dab_status_t dab_selftest_mma(int d, const void* x, const void* y, const void* z
   else
     e = cudaLaunchKernel(dab::selftest_kernel_ptr<64>(), dim3(1), dim3(192), args,
                          dab::selftest_smem_bytes<64>(), stream);
+  return e == cudaSuccess ? DAB_OK : DAB_ERR_CUDA;
+}
+
+// ------------------------------------------------------------- tensor peak
+int dab_mma_peak_grid(void) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return sms;
+}
+
+dab_status_t dab_mma_peak(int iters, void* status_ws, cudaStream_t stream) {
+  if (iters < 1 || iters > (1 << 22) || !aligned16(status_ws)) return DAB_ERR_INVALID_ARG;
+  if (!device_setup(nullptr, nullptr)) return DAB_ERR_UNSUPPORTED;
+  const int grid = dab_mma_peak_grid();
+  if (grid <= 0) return DAB_ERR_CUDA;
+  if (cudaMemsetAsync(status_ws, 0, 16, stream) != cudaSuccess) return DAB_ERR_CUDA;
+  dab::WsHeader* hdr = static_cast<dab::WsHeader*>(status_ws);
+  unsigned long long timeout_ns = 4000000000ull;  // the longest allowed run is about 1 s
+  void* args[] = {&iters, &hdr, &timeout_ns};
+  const cudaError_t e = cudaLaunchKernel(dab::peak_kernel_ptr(), dim3(grid), dim3(dab::peak_threads()),
+                                         args, dab::peak_smem_bytes(), stream);
   return e == cudaSuccess ? DAB_OK : DAB_ERR_CUDA;
 }
 

@@ -497,6 +497,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     const int r = quad * 32 + lane;                     // d index (d = 128) or Q row (d = 64)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     constexpr int kVals = (HD == 128) ? 64 : 32;        // values per thread per step
+    // Inside a unit, a step's contribution is published (fence, then release
+    // of the semaphore) only after the next step's partial has been drained:
+    // the fence waits for the adds to complete, and draining first frees the
+    // tensor memory for the next dP without waiting for that.  The last step
+    // of a unit publishes at once.
+    uint32_t* pend_sem = nullptr;
+    uint32_t pend_val = 0;
     int s = 0, uidx = 0;
     bool ok = true;
     while (ok) {
@@ -533,6 +540,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->dq_empty);
+        if (pend_sem != nullptr) {  // publish the previous step's contribution
+          fence_acq_rel_gpu();
+          __syncwarp();
+          if (lane == 0) st_release_gpu(pend_sem, pend_val);
+          pend_sem = nullptr;
+        }
         if (deterministic) {
           int g = 1;
           if (lane == 0) g = sem_wait(sem, (uint32_t)lrank, wc, sem_detail) ? 1 : 0;
@@ -567,9 +580,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         if (deterministic) {
           // Publish: the warp's writes are ordered before the release of
           // rank + 1 (fence per lane, warp barrier, lane 0's release store).
-          fence_acq_rel_gpu();
-          __syncwarp();
-          if (lane == 0) st_release_gpu(sem, (uint32_t)lrank + 1u);
+          // (rank + 1 is released after the next step's drain, see above)
+          if (t + 1 < steps) {
+            pend_sem = sem;
+            pend_val = (uint32_t)lrank + 1u;
+          } else {
+            fence_acq_rel_gpu();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(sem, (uint32_t)lrank + 1u);
+          }
         }
         ++s;
       }

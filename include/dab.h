@@ -154,6 +154,10 @@ typedef struct {
 #define DAB_BWD_SKIP_PREPROCESS 0x1u
 /* Skip the convert kernel (dQ is left in the workspace accumulator).        */
 #define DAB_BWD_SKIP_CONVERT 0x2u
+/* Skip the main kernel (measurement only: with DAB_BWD_SKIP_PREPROCESS it
+ * runs the convert kernel alone, so that its time can be taken; dQ, dK and
+ * dV are then not the gradients).                                          */
+#define DAB_BWD_SKIP_MAIN 0x4u
 
 dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v,
                              const void* o, const float* lse, const void* dout,

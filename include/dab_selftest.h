@@ -30,6 +30,22 @@ dab_status_t dab_selftest_mma(int d, const void* x, const void* y, const void* z
                               const void* pm, float* out0, float* out1, float* out2,
                               float* out3, void* status_ws, cudaStream_t stream);
 
+/* Dense bf16 tensor throughput of this build's own tcgen05 path, the
+ * denominator against which the backward's throughput is quoted as a fraction
+ * of the tensor peak.  Launches one CTA per SM; each issues `iters` x 4
+ * back-to-back tcgen05.mma of M = 128, N = 256, K = 16 (bf16 x bf16 -> f32 in
+ * tensor memory) from operands resident in shared memory, so the work is
+ *     (SM count) * iters * 4 * 2 * 128 * 256 * 16  flops
+ * and the caller times the launch on `stream` (CUDA events).  iters in
+ * [1, 1<<22] (about a second at most).  status_ws: >= 256 bytes of device memory, caller-owned; its
+ * status word (dab_check_status) reports a timed-out wait.  Asynchronous;
+ * argument errors are returned synchronously.  Not part of the attention
+ * operation; the paper has no counterpart.                                  */
+dab_status_t dab_mma_peak(int iters, void* status_ws, cudaStream_t stream);
+
+/* The SM count dab_mma_peak launches on (the current device), or -1.       */
+int dab_mma_peak_grid(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -86,3 +86,7 @@ def test_bad_arguments_rejected_without_touching_the_device(lib):
     assert lib.dab_attn_fwd(nul, p, p, p, p, 1, 1, 128, 64, 0.125, 0, nul, 0, None) == 1
     assert lib.dab_attn_fwd(p, p, p, p, p, 1, 1, 128, 64, 0.125, 3, nul, 0, None) == 1
     assert lib.dab_check_status(nul, None) == 1
+    # tensor-peak measurement: iteration count and status buffer are checked first
+    assert lib.dab_mma_peak(0, p, None) == 1
+    assert lib.dab_mma_peak(1 << 23, p, None) == 1
+    assert lib.dab_mma_peak(1000, ctypes.c_void_p(17), None) == 1

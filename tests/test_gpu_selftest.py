@@ -19,3 +19,14 @@ def test_mma_operand_forms(d):
     for n, (got, w) in enumerate(zip(outs, want)):
         err = (got.cpu().double() - w).abs().max().item() / w.abs().max().item()
         assert err < 1e-5, f"form {n}: rel err {err:.3e}"
+
+
+@pytest.mark.gpu
+def test_mma_peak_is_a_plausible_tensor_rate():
+    """The build's own tcgen05 throughput measurement: positive, completes
+    without a device error, and below the nominal dense bf16 rate of the chip
+    at its highest clock (8192 flops per clock per SM)."""
+    r = dab.mma_peak(iters=20000)
+    sms = r["grid"]
+    ceiling = sms * 8192 * 2.2e9 / 1e12   # TFLOP/s at 2.2 GHz, above any clock the part runs
+    assert 0.3 * ceiling < r["tflops"] < ceiling, r
