@@ -322,6 +322,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                                    "128x256x16 from shared memory"},
         "side_kernels": side,
         "per_schedule": per,
+        "auto_schedules": {m: dab.sched_select(m, B, H, S,
+                                               torch.cuda.get_device_properties(dev).multi_processor_count)
+                           for m in MASKS},
         "e2e": {"value": round(world * step_flops / (e2e_ms * 1e9), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},

@@ -18,7 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdab.so")
 
 MASKS = {"full": 0, "causal": 1}
-SCHEDS = {"serial": 0, "descending": 1, "descending_q": 1, "shift": 2, "atomic": 3}
+SCHEDS = {"serial": 0, "descending": 1, "descending_q": 1, "shift": 2, "atomic": 3, "auto": 4}
 SCHED_NAMES = ("serial", "descending_q", "shift", "atomic")
 STATUS = {0: "DAB_OK", 1: "DAB_ERR_INVALID_ARG", 2: "DAB_ERR_UNSUPPORTED", 3: "DAB_ERR_WORKSPACE",
           4: "DAB_ERR_CUDA", 5: "DAB_ERR_TIMEOUT", 6: "DAB_ERR_DEVICE_BOUNDS"}
@@ -31,6 +31,7 @@ EXPORTED = (
     "dab_status_string", "dab_attn_bwd_ex", "dab_bwd_preprocess", "dab_bwd_workspace_layout",
     "dab_sched_units_per_head", "dab_sched_unit_steps", "dab_sched_step", "dab_sched_rank",
     "dab_sched_contributors", "dab_sched_gang_size", "dab_dag_simulate", "dab_dag_critical_path",
+    "dab_dag_simulate_ways", "dab_sched_select",
     "dab_selftest_mma", "dab_last_error_string", "dab_attn_bwd_noalloc", "dab_mma_peak",
     "dab_mma_peak_grid",
 )
@@ -101,6 +102,10 @@ def load_library(path: str = LIB_PATH):
     dp = ctypes.POINTER(ctypes.c_double)
     lib.dab_dag_simulate.argtypes = [i, i, i, i, i, ctypes.c_double, ctypes.c_double, i, dp, dp]
     lib.dab_dag_simulate.restype = i
+    lib.dab_dag_simulate_ways.argtypes = [i, i, i, i, i, ctypes.c_double, ctypes.c_double, i, i, dp, dp]
+    lib.dab_dag_simulate_ways.restype = i
+    lib.dab_sched_select.argtypes = [i] * 5
+    lib.dab_sched_select.restype = i
     lib.dab_dag_critical_path.argtypes = [i, i, i, ctypes.c_double, ctypes.c_double, i]
     lib.dab_dag_critical_path.restype = ctypes.c_double
     lib.dab_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 4 + [f, i, i, vp]
@@ -258,12 +263,22 @@ def sched_gang_size(sched, mask, N) -> int:
     return load_library().dab_sched_gang_size(_sched(sched), _mask(mask), N)
 
 
-def dag_simulate(sched, mask, N, heads, ctas, wc=1.0, wr=0.0, reducer_depth=0):
+def dag_simulate(sched, mask, N, heads, ctas, wc=1.0, wr=0.0, reducer_depth=0, ways=1):
     """(status, makespan, busy_fraction) of the schedule's DAG model."""
     mk, busy = ctypes.c_double(), ctypes.c_double()
-    rc = load_library().dab_dag_simulate(_sched(sched), _mask(mask), N, heads, ctas, wc, wr,
-                                         reducer_depth, ctypes.byref(mk), ctypes.byref(busy))
+    rc = load_library().dab_dag_simulate_ways(_sched(sched), _mask(mask), N, heads, ctas, wc, wr,
+                                              reducer_depth, ways, ctypes.byref(mk),
+                                              ctypes.byref(busy))
     return rc, mk.value, busy.value
+
+
+def sched_select(mask, B: int, H: int, S: int, ctas: int) -> str:
+    """The deterministic schedule the library runs for DAB_SCHED_AUTO on
+    `ctas` CTAs (the SM count of the device)."""
+    r = load_library().dab_sched_select(_mask(mask), B, H, S, ctas)
+    if r < 0:
+        raise DabError(1, "dab_sched_select")
+    return SCHED_NAMES[r]
 
 
 def dag_critical_path(sched, mask, N, wc=1.0, wr=0.0, reducer_depth=0) -> float:

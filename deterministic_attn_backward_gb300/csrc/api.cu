@@ -140,6 +140,26 @@ dab_status_t check_enums(dab_mask_t mask, dab_sched_t sched) {
   return DAB_OK;
 }
 
+// The entry points that run a backward also take DAB_SCHED_AUTO.
+dab_status_t check_enums_auto(dab_mask_t mask, dab_sched_t sched) {
+  return sched == DAB_SCHED_AUTO ? check_enums(mask, DAB_SCHED_SERIAL) : check_enums(mask, sched);
+}
+
+// DAB_SCHED_AUTO -> the schedule that dab_sched_select picks for `ctas` CTAs
+// (the SM count of the current device when ctas <= 0).
+dab_status_t resolve_sched(dab_mask_t mask, int B, int H, int S, int ctas, dab_sched_t* sched) {
+  if (*sched != DAB_SCHED_AUTO) return DAB_OK;
+  if (ctas <= 0) {
+    int sms = 0;
+    if (!device_setup(nullptr, &sms)) return DAB_ERR_UNSUPPORTED;
+    ctas = sms;
+  }
+  const int pick = dab_sched_select(mask, B, H, S, ctas);
+  if (pick < 0) return DAB_ERR_INVALID_ARG;
+  *sched = static_cast<dab_sched_t>(pick);
+  return DAB_OK;
+}
+
 int acc_ways(dab_sched_t sched) { return sched == DAB_SCHED_ATOMIC ? 1 : dab::kAccWays; }
 
 bool layout(int B, int H, int S, int d, dab_sched_t sched, dab_ws_layout_t* L) {
@@ -189,7 +209,9 @@ const char* dab_status_string(dab_status_t s) {
 
 dab_status_t dab_bwd_workspace_layout(int B, int H, int S, int d, dab_mask_t mask, dab_sched_t sched,
                                       dab_ws_layout_t* L) {
-  if (L == nullptr || check_enums(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
+  if (L == nullptr || check_enums_auto(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
+  // every deterministic schedule has the same layout, so AUTO needs no device
+  if (sched == DAB_SCHED_AUTO) sched = DAB_SCHED_DESCENDING_Q;
   return layout(B, H, S, d, sched, L) ? DAB_OK : DAB_ERR_INVALID_ARG;
 }
 
@@ -237,8 +259,9 @@ dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v, void* o, 
 dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dout, int B, int H, int S,
                                 int d, dab_mask_t mask, dab_sched_t sched, void* workspace,
                                 size_t ws_bytes, cudaStream_t stream) {
-  if (check_shape(B, H, S, d) != DAB_OK || check_enums(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
+  if (check_shape(B, H, S, d) != DAB_OK || check_enums_auto(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
   if (!aligned16(o) || !aligned16(lse) || !aligned16(dout)) return DAB_ERR_INVALID_ARG;
+  if (sched == DAB_SCHED_AUTO) sched = DAB_SCHED_DESCENDING_Q;  // same preprocessing for all ordered schedules
   dab_ws_layout_t L;
   layout(B, H, S, d, sched, &L);
   if (workspace == nullptr || !aligned16(workspace)) return DAB_ERR_WORKSPACE;
@@ -262,11 +285,15 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
                              int H, int S, int d, float scale, dab_mask_t mask, dab_sched_t sched,
                              void* workspace, size_t ws_bytes, cudaStream_t stream,
                              const dab_bwd_opts_t* opts) {
-  if (check_shape(B, H, S, d) != DAB_OK || check_enums(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
+  if (check_shape(B, H, S, d) != DAB_OK || check_enums_auto(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return DAB_ERR_INVALID_ARG;
   if (!(scale > 0.f)) return DAB_ERR_INVALID_ARG;
+  {
+    const dab_status_t st = resolve_sched(mask, B, H, S, (opts && opts->grid > 0) ? opts->grid : 0, &sched);
+    if (st != DAB_OK) return st;
+  }
   const int N = S / 128;
   if (sched == DAB_SCHED_SHIFT && mask == DAB_MASK_CAUSAL && (N % 2) != 0) return DAB_ERR_UNSUPPORTED;
   dab_ws_layout_t L;

@@ -15,10 +15,15 @@
 //   R(U,t-1) -> C(U,t)      reducer_depth 0   (reduction inside the chain)
 //   R(U,t-1-k) -> C(U,t)    reducer_depth k   (k reductions may trail)
 //   C(U,t) -> R(U,t),  R(U,t-1) -> R(U,t)     (one reducer per CTA)
-//   R(rank-1 contributor of dQ_j) -> R(U,t)   (fixed reduction order)
+//   R(rank-w contributor of dQ_j) -> R(U,t)   (fixed reduction order; with
+//                                             w interleaved accumulation
+//                                             buffers, rank r follows r - w)
 //   last C / R of the previous unit on the same CTA -> first C / R of U.
 #include <algorithm>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "tile_sched.h"
@@ -28,6 +33,7 @@ namespace {
 struct Problem {
   int sched, mask, N, heads, ctas, reducer_depth;
   double wc, wr;
+  int ways = 1;                   // interleaved accumulation buffers
   int uph = 0;                    // units per head
   int total = 0;                  // units overall
   std::vector<int> step_off;      // node offset of unit U's first step
@@ -81,8 +87,8 @@ bool build(Problem& P) {
 
 int rank_pred(const Problem& P, int n) {
   const int r = P.node_rank[n];
-  if (r <= 0) return -1;
-  return P.rank_node[((size_t)P.node_head[n] * P.N + P.node_q[n]) * P.N + (r - 1)];
+  if (r < P.ways) return -1;
+  return P.rank_node[((size_t)P.node_head[n] * P.N + P.node_q[n]) * P.N + (r - P.ways)];
 }
 
 // Static placement (unit U on CTA U mod ctas, ascending U): longest paths
@@ -180,11 +186,12 @@ bool run_dynamic(const Problem& P, double* makespan) {
 
 }  // namespace
 
-extern "C" int dab_dag_simulate(int sched, int mask, int N, int heads, int ctas,
-                                double wc, double wr, int reducer_depth,
-                                double* makespan, double* busy_fraction) {
-  if (sched < 0 || sched > 3 || mask < 0 || mask > 1 || wc < 0 || wr < 0) return -1;
+extern "C" int dab_dag_simulate_ways(int sched, int mask, int N, int heads, int ctas,
+                                     double wc, double wr, int reducer_depth, int ways,
+                                     double* makespan, double* busy_fraction) {
+  if (sched < 0 || sched > 3 || mask < 0 || mask > 1 || wc < 0 || wr < 0 || ways < 1) return -1;
   Problem P{sched, mask, N, heads, ctas, reducer_depth, wc, wr};
+  P.ways = ways;
   if (!build(P)) return -1;
   double mk = 0.0;
   bool ok;
@@ -202,6 +209,13 @@ extern "C" int dab_dag_simulate(int sched, int mask, int N, int heads, int ctas,
   return 0;
 }
 
+extern "C" int dab_dag_simulate(int sched, int mask, int N, int heads, int ctas,
+                                double wc, double wr, int reducer_depth,
+                                double* makespan, double* busy_fraction) {
+  return dab_dag_simulate_ways(sched, mask, N, heads, ctas, wc, wr, reducer_depth, 1, makespan,
+                               busy_fraction);
+}
+
 extern "C" double dab_dag_critical_path(int sched, int mask, int N, double wc, double wr,
                                         int reducer_depth) {
   Problem P{sched, mask, N, 1, 1, reducer_depth, wc, wr};
@@ -211,3 +225,52 @@ extern "C" double dab_dag_critical_path(int sched, int mask, int N, double wc, d
   if (!run_static(P, &mk)) return -2.0;
   return mk;
 }
+
+// Schedule selection (the "palette" of DASH, technical summary section 4:
+// the best schedule depends on the mask and the problem shape).  The DAG
+// model above, with the weights that match the GB300 measurements of this
+// library (reduction phase as long as a compute phase, one reduction
+// trailing the compute, four interleaved accumulation buffers), picks the
+// deterministic schedule with the smallest predicted makespan.  Ties go to
+// DESCENDING_Q, then SERIAL, then SHIFT.  Results are cached.
+extern "C" int dab_sched_select(int mask, int B, int H, int S, int ctas) {
+  if (mask < 0 || mask > 1 || B < 1 || H < 1 || S < 128 || (S % 128) != 0 || ctas < 1) return -1;
+  const int N = S / 128;
+  const long long bh = (long long)B * H;
+  static std::mutex mu;
+  static std::map<std::tuple<int, long long, int, int>, int> cache;
+  const auto key = std::make_tuple(mask, bh, N, ctas);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  constexpr double kWc = 1.0, kWr = 1.0;
+  constexpr int kDepth = 1, kWays = 4;
+  const int order[3] = {dab::kSchedDescending, dab::kSchedSerial, dab::kSchedShift};
+  int best = dab::kSchedDescending;
+  double best_mk = -1.0;
+  for (int sched : order) {
+    if (sched == dab::kSchedShift && mask == dab::kMaskCausal && (N % 2) != 0) continue;
+    if (dab::gang_size(sched, mask, N) > ctas) continue;
+    const int uph = dab::units_per_head(sched, mask, N);
+    // All heads up to a budget of ~1.5M DAG nodes (the placement of units
+    // on CTAs repeats only after many heads, and it decides whether a shift
+    // gang is split between rounds), but at least enough to fill the CTAs
+    // twice.
+    const long long fill = (2LL * ctas + uph - 1) / uph;
+    const long long budget = 1500000LL / ((long long)N * N);
+    const int heads = (int)std::min<long long>(bh, std::max<long long>({1LL, fill, budget}));
+    double mk = 0.0;
+    if (dab_dag_simulate_ways(sched, mask, N, heads, ctas, kWc, kWr, kDepth, kWays, &mk, nullptr) != 0)
+      continue;
+    if (best_mk < 0.0 || mk < best_mk * (1.0 - 1e-9)) {
+      best = sched;
+      best_mk = mk;
+    }
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = best;
+  return best;
+}
+

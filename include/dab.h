@@ -70,7 +70,13 @@ typedef enum {
     DAB_SCHED_SERIAL = 0,
     DAB_SCHED_DESCENDING_Q = 1,
     DAB_SCHED_SHIFT = 2,
-    DAB_SCHED_ATOMIC = 3
+    DAB_SCHED_ATOMIC = 3,
+    /* Accepted by dab_bwd_workspace_size, dab_bwd_workspace_layout,
+     * dab_bwd_preprocess, dab_attn_bwd and dab_attn_bwd_ex only: the library
+     * runs the deterministic schedule that dab_sched_select() picks for the
+     * problem on the current device (the choice depends on mask, B*H, S and
+     * the SM count, never on the data, so repeated calls give the same bits). */
+    DAB_SCHED_AUTO = 4
 } dab_sched_t;
 
 typedef enum {
@@ -258,6 +264,24 @@ int dab_sched_gang_size(dab_sched_t sched, dab_mask_t mask, int N);
 int dab_dag_simulate(dab_sched_t sched, dab_mask_t mask, int N, int heads,
                      int ctas, double wc, double wr, int reducer_depth,
                      double* makespan, double* busy_fraction);
+
+/* The same model with `ways` interleaved accumulation buffers per dQ tile
+ * (the main kernel uses four for the ordered schedules): the reduction of
+ * rank r waits only for that of rank r - ways.  ways = 1 is
+ * dab_dag_simulate().                                                       */
+int dab_dag_simulate_ways(dab_sched_t sched, dab_mask_t mask, int N, int heads,
+                          int ctas, double wc, double wr, int reducer_depth,
+                          int ways, double* makespan, double* busy_fraction);
+
+/* Schedule selection, the "palette" of DASH (technical summary section 4:
+ * which schedule is best depends on the mask and the shape).  Returns the
+ * deterministic schedule (SERIAL, DESCENDING_Q or SHIFT) with the smallest
+ * makespan in the DAG model of dab_dag_simulate_ways() for B*H heads of
+ * S/128 tiles on `ctas` CTAs, with weights fitted to this library's GB300
+ * measurements (wr = wc, reducer_depth 1, 4 buffers); ties go to
+ * DESCENDING_Q, then SERIAL.  Host only, no CUDA call; -1 on bad arguments.
+ * Results are cached per (mask, B*H, S, ctas); thread-safe.                 */
+int dab_sched_select(dab_mask_t mask, int B, int H, int S, int ctas);
 
 /* Longest path of one head's DAG with one processor per unit.               */
 double dab_dag_critical_path(dab_sched_t sched, dab_mask_t mask, int N,

@@ -44,6 +44,13 @@ def test_status_strings(lib):
         assert lib.dab_status_string(code).decode() == name
 
 
+def test_auto_schedule_workspace_is_the_ordered_one(lib):
+    for B, H, S, d in ((1, 1, 128, 64), (2, 16, 8192, 128)):
+        for mask in (0, 1):
+            assert lib.dab_bwd_workspace_size(B, H, S, d, mask, 4) == lib.dab_bwd_workspace_size(
+                B, H, S, d, mask, 1) > 0
+
+
 def test_workspace_layout(lib):
     B, H, S, d = 2, 16, 8192, 128
     L = dab.workspace_layout(B, H, S, d, "causal", "descending_q")
@@ -86,6 +93,11 @@ def test_bad_arguments_rejected_without_touching_the_device(lib):
     assert lib.dab_attn_fwd(nul, p, p, p, p, 1, 1, 128, 64, 0.125, 0, nul, 0, None) == 1
     assert lib.dab_attn_fwd(p, p, p, p, p, 1, 1, 128, 64, 0.125, 3, nul, 0, None) == 1
     assert lib.dab_check_status(nul, None) == 1
+    # DAB_SCHED_AUTO (4): accepted by the backward entry points, not by the
+    # schedule introspection functions
+    assert lib.dab_sched_units_per_head(4, 0, 8) == -1
+    assert call(p, p, p, p, p, p, p, p, p, 1, 1, 192, 64, 0.125, 0, 4, p, big, None) == 1
+    assert call(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 5, p, big, None) == 1
     # tensor-peak measurement: iteration count and status buffer are checked first
     assert lib.dab_mma_peak(0, p, None) == 1
     assert lib.dab_mma_peak(1 << 23, p, None) == 1

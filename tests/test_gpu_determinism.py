@@ -44,3 +44,19 @@ def test_descending_keeps_serial_dq_bits(mask, d):
     for x, y in zip(a[1:], b[1:]):
         err = (x.double() - y.double()).abs().max() / y.double().abs().max()
         assert err < 1e-2
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape,mask", [((2, 4, 1024, 64), "full"), ((2, 4, 1024, 128), "causal"),
+                                        ((1, 3, 2048, 128), "full")])
+def test_auto_runs_the_selected_schedule(shape, mask):
+    """DAB_SCHED_AUTO runs the schedule dab_sched_select picks for this
+    device's SM count: the same bits as asking for it by name, every time."""
+    B, H, S, d = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pick = dab.sched_select(mask, B, H, S, sms)
+    auto = _grads(B, H, S, d, mask, "auto", 2)
+    named = _grads(B, H, S, d, mask, pick, 1)[0]
+    for run in auto:
+        for a, b in zip(run, named):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))

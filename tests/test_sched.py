@@ -179,3 +179,58 @@ def test_schedules_recover_utilisation():
     assert busy("descending_q", "causal", 0.3) > busy("serial", "causal", 0.3) + 0.1
     assert busy("shift", "full", 1.2) > busy("serial", "full", 1.2) + 0.05
     assert busy("atomic", "full", 0.3) > 0.95
+
+
+# ---------------------------------------------------------------- palette
+def test_interleaved_buffers_in_the_dag_model():
+    """ways = 1 is the plain model; with as many buffers as contributors no
+    reduction waits on another, so an ordered schedule takes exactly as long
+    as the unordered one with the same step order and dispatch."""
+    for mask in ("full", "causal"):
+        for N in (4, 8):
+            a = dab.dag_simulate("serial", mask, N, 3, 5, 1.0, 0.7, 1, ways=1)
+            b = dab.dag_simulate("serial", mask, N, 3, 5, 1.0, 0.7, 1)
+            assert a == b
+            free = dab.dag_simulate("serial", mask, N, 3, 5, 1.0, 0.7, 1, ways=N)
+            unordered = dab.dag_simulate("atomic", mask, N, 3, 5, 1.0, 0.7, 1)
+            assert free[0] == 0 and abs(free[1] - unordered[1]) < 1e-9
+            # more buffers never lengthen the makespan
+            m = [dab.dag_simulate("descending_q", mask, N, 3, 5, 1.0, 0.7, 1, ways=w)[1]
+                 for w in (1, 2, 4)]
+            assert m[0] >= m[1] - 1e-9 >= m[2] - 2e-9
+
+
+def test_sched_select_picks_a_runnable_deterministic_schedule():
+    lib = dab.load_library()
+    for mask in ("full", "causal"):
+        for B, H, S in ((1, 2, 256), (2, 3, 384), (4, 16, 2048), (2, 16, 8192)):
+            for ctas in (4, 37, 152):
+                pick = dab.sched_select(mask, B, H, S, ctas)
+                assert pick in ("serial", "descending_q", "shift")
+                N = S // 128
+                if pick == "shift":
+                    assert not (mask == "causal" and N % 2)
+                    assert dab.sched_gang_size("shift", mask, N) <= ctas
+                # deterministic and cached: the same answer again
+                assert dab.sched_select(mask, B, H, S, ctas) == pick
+    # no SHIFT when its gang cannot be resident, odd causal N never SHIFT
+    assert dab.sched_select("full", 1, 1, 128 * 64, 8) != "shift"
+    assert dab.sched_select("causal", 1, 4, 384, 152) != "shift"
+    # bad arguments
+    assert lib.dab_sched_select(2, 1, 1, 256, 152) == -1
+    assert lib.dab_sched_select(0, 1, 1, 200, 152) == -1
+    assert lib.dab_sched_select(0, 1, 1, 256, 0) == -1
+
+
+def test_sched_select_follows_the_model():
+    """The pick is the model's argmin (ties to descending_q, then serial)."""
+    for mask, B, H, S in (("causal", 2, 4, 2048), ("full", 1, 8, 4096)):
+        N = S // 128
+        mk = {}
+        for s in ("descending_q", "serial", "shift"):
+            rc, m, _ = dab.dag_simulate(s, mask, N, B * H, 152, 1.0, 1.0, 1, ways=4)
+            if rc == 0 and dab.sched_gang_size(s, mask, N) <= 152:
+                mk[s] = m
+        best = min(mk.values())
+        expect = next(s for s in ("descending_q", "serial", "shift") if s in mk and mk[s] <= best * (1 + 1e-9))
+        assert dab.sched_select(mask, B, H, S, 152) == expect
