@@ -31,7 +31,7 @@ EXPORTED = (
     "dab_status_string", "dab_attn_bwd_ex", "dab_bwd_preprocess", "dab_bwd_workspace_layout",
     "dab_sched_units_per_head", "dab_sched_unit_steps", "dab_sched_step", "dab_sched_rank",
     "dab_sched_contributors", "dab_sched_gang_size", "dab_dag_simulate", "dab_dag_critical_path",
-    "dab_dag_simulate_ways", "dab_sched_select",
+    "dab_dag_simulate_ways", "dab_sched_select", "dab_attn_bwd_host", "dab_bwd_host_workspace_size",
     "dab_selftest_mma", "dab_last_error_string", "dab_attn_bwd_noalloc", "dab_mma_peak",
     "dab_mma_peak_grid",
 )
@@ -106,6 +106,10 @@ def load_library(path: str = LIB_PATH):
     lib.dab_dag_simulate_ways.restype = i
     lib.dab_sched_select.argtypes = [i] * 5
     lib.dab_sched_select.restype = i
+    lib.dab_bwd_host_workspace_size.argtypes = [i] * 7
+    lib.dab_bwd_host_workspace_size.restype = sz
+    lib.dab_attn_bwd_host.argtypes = [vp] * 9 + [i] * 4 + [f, i, i, vp, sz, i, vp]
+    lib.dab_attn_bwd_host.restype = i
     lib.dab_dag_critical_path.argtypes = [i, i, i, ctypes.c_double, ctypes.c_double, i]
     lib.dab_dag_critical_path.restype = ctypes.c_double
     lib.dab_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 4 + [f, i, i, vp]
@@ -184,17 +188,63 @@ def attn_fwd(q, k, v, mask="full", scale=None, workspace=None, out=None, lse=Non
     return o, lse_t
 
 
+def host_workspace_size(B, H, S, d, mask="full", sched="serial", chunks=0) -> int:
+    n = load_library().dab_bwd_host_workspace_size(B, H, S, d, _mask(mask), _sched(sched), chunks)
+    if n == 0:
+        raise DabError(1, "dab_bwd_host_workspace_size")
+    return n
+
+
+def new_host_workspace(B, H, S, d, mask="full", sched="serial", chunks=0, device="cuda"):
+    """Device workspace of the host-buffer path (dab_attn_bwd_host)."""
+    return torch.empty(host_workspace_size(B, H, S, d, mask, sched, chunks), dtype=torch.uint8,
+                       device=device)
+
+
+def _attn_bwd_host(q, k, v, o, lse, dout, mask, sched, scale, workspace, out, chunks):
+    """CPU tensors through dab_attn_bwd_host (copies overlapped with the
+    computation inside the library); returns once the gradients are in host
+    memory.  Pinned inputs and outputs give asynchronous copies."""
+    lib = load_library()
+    B, H, S, d = _shape(q)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v, o, dout = (t.contiguous() if t.dtype == torch.bfloat16 else t.to(torch.bfloat16).contiguous()
+                        for t in (q, k, v, o, dout))
+    lse = lse.contiguous()
+    if lse.dtype != torch.float32:
+        raise TypeError("lse must be float32")
+    if workspace is None:
+        workspace = new_host_workspace(B, H, S, d, mask, sched, chunks, dev)
+    if out is None:
+        out = tuple(torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(3))
+    dq, dk, dv = out
+    _check(lib.dab_attn_bwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                 dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, d,
+                                 float(scale if scale is not None else default_scale(d)), _mask(mask),
+                                 _sched(sched), workspace.data_ptr(), workspace.numel(), chunks,
+                                 _stream(dev)), "dab_attn_bwd_host")
+    torch.cuda.current_stream(dev).synchronize()
+    return dq, dk, dv
+
+
 def attn_bwd(q, k, v, o, lse, dout, mask="full", sched="serial", scale=None, workspace=None,
-             out=None, opts: BwdOpts | None = None):
+             out=None, opts: BwdOpts | None = None, chunks: int = 0):
     """dQ, dK, dV (bf16 [B,H,S,d]) through the C ABI.
 
-    Device tensors are used in place.  CPU tensors are copied to the device
-    first and the gradients are copied back (the end-to-end path).
+    Device tensors are used in place (dab_attn_bwd / dab_attn_bwd_ex).  CPU
+    tensors go through dab_attn_bwd_host, which copies them to the device
+    and the gradients back, overlapped with the computation in `chunks`
+    groups of heads (0 = the library's default); `workspace` is then the
+    device workspace of new_host_workspace() and `out` host tensors.
     """
     lib = load_library()
     B, H, S, d = _shape(q)
     host = not q.is_cuda
-    dev = torch.device("cuda") if host else q.device
+    if host:
+        if opts is not None:
+            raise ValueError("opts apply to device tensors only")
+        return _attn_bwd_host(q, k, v, o, lse, dout, mask, sched, scale, workspace, out, chunks)
+    dev = q.device
     q, k, v, o, dout = (_dev_bf16(t, dev) for t in (q, k, v, o, dout))
     lse = lse.to(dev, non_blocking=True).contiguous()
     if lse.dtype != torch.float32:
@@ -212,8 +262,6 @@ def attn_bwd(q, k, v, o, lse, dout, mask="full", sched="serial", scale=None, wor
         _check(lib.dab_attn_bwd(*args), "dab_attn_bwd")
     else:
         _check(lib.dab_attn_bwd_ex(*args, ctypes.byref(opts)), "dab_attn_bwd_ex")
-    if host:
-        return dq.cpu(), dk.cpu(), dv.cpu()
     return dq, dk, dv
 
 

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libdab.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["api.cu", "bwd.cu", "fwd.cu", "aux.cu", "selftest.cu", "dagsim.cpp", "noalloc.cu", "peak.cu"]
+SOURCES = ["api.cu", "bwd.cu", "fwd.cu", "aux.cu", "selftest.cu", "dagsim.cpp", "noalloc.cu", "peak.cu", "hostio.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

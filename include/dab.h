@@ -233,6 +233,37 @@ dab_status_t dab_attn_bwd_noalloc(const void* q, const void* k, const void* v,
                                   cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* The backward on HOST buffers, with the host<->device copies overlapped with
+ * the computation.  Not on the pages: it is the path of a caller whose
+ * tensors live in host memory.  q, k, v, o, dout (bf16 [B][H][S][d]) and lse
+ * (f32 [B][H][S]) are read from host memory, dq, dk, dv (bf16) written to
+ * host memory; for overlapped (asynchronous) copies all nine must be pinned
+ * (cudaHostAlloc / cudaHostRegister), otherwise the copies are synchronous.
+ * The heads are split into `chunks` groups of consecutive (b, h) heads (0 =
+ * the default, 8; at most B*H): the inputs of all groups are copied in back
+ * to back on a library-owned stream, each group's backward runs on `stream`
+ * as dab_attn_bwd on that range of heads (so its results are those of
+ * dab_attn_bwd for an explicit schedule; DAB_SCHED_AUTO picks per group
+ * shape), and each group's gradients are copied back on a second
+ * library-owned stream while the next group computes.  Everything starts
+ * after the work already queued on `stream`, and `stream` waits for the last
+ * copy back: synchronise `stream` before reading dq, dk, dv or reusing the
+ * inputs.  dev_ws: device memory of dab_bwd_host_workspace_size() bytes,
+ * 256-byte aligned, caller-owned (copies of inputs and outputs, and the
+ * backward workspace of one group).  Errors as dab_attn_bwd; on an error
+ * after the first group was queued, earlier groups may still complete.      */
+size_t dab_bwd_host_workspace_size(int B, int H, int S, int d, dab_mask_t mask,
+                                   dab_sched_t sched, int chunks);
+
+dab_status_t dab_attn_bwd_host(const void* q, const void* k, const void* v,
+                               const void* o, const float* lse, const void* dout,
+                               void* dq, void* dk, void* dv,
+                               int B, int H, int S, int d, float scale,
+                               dab_mask_t mask, dab_sched_t sched,
+                               void* dev_ws, size_t dev_ws_bytes, int chunks,
+                               cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Schedule introspection (host only, no GPU needed).  N = S/128 tiles.
  * These are the same functions the main kernel evaluates on the device.     */
 

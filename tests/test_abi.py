@@ -98,6 +98,17 @@ def test_bad_arguments_rejected_without_touching_the_device(lib):
     assert lib.dab_sched_units_per_head(4, 0, 8) == -1
     assert call(p, p, p, p, p, p, p, p, p, 1, 1, 192, 64, 0.125, 0, 4, p, big, None) == 1
     assert call(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 5, p, big, None) == 1
+    # host-buffer path: sizes, null pointers and workspace checked before any CUDA call
+    assert lib.dab_bwd_host_workspace_size(2, 3, 640, 128, 0, 0, 2) > lib.dab_bwd_workspace_size(
+        1, 3, 640, 128, 0, 0)
+    assert lib.dab_bwd_host_workspace_size(2, 3, 600, 128, 0, 0, 2) == 0
+    assert lib.dab_bwd_host_workspace_size(2, 3, 640, 80, 0, 0, 2) == 0
+    hcall = lambda *a: lib.dab_attn_bwd_host(*a)
+    assert hcall(nul, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, p, big, 0, None) == 1
+    assert hcall(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, nul, big, 0, None) == 3
+    assert hcall(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, p, 64, 0, None) == 3
+    assert hcall(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, ctypes.c_void_p(16 + 256), big,
+                 0, None) == 3
     # tensor-peak measurement: iteration count and status buffer are checked first
     assert lib.dab_mma_peak(0, p, None) == 1
     assert lib.dab_mma_peak(1 << 23, p, None) == 1
