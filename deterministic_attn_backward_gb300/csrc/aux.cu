@@ -94,10 +94,18 @@ __global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__
       const int j = (int)((row % S) / kTile);
       if (j + 1 < nacc) nacc = j + 1;
     }
-    float4 v = acc[i];
-    for (int m = 1; m < nacc; ++m) {  // fixed order: buffer 0, 1, ...
-      const float4 w = acc[i + (long long)m * acc_stride_vec4];
-      v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+    // all loads first (at most kAccWays buffers), then the sum in the
+    // fixed order buffer 0, 1, ...
+    float4 w[kAccWays];
+#pragma unroll
+    for (int m = 0; m < kAccWays; ++m)
+      if (m < nacc) w[m] = acc[i + (long long)m * acc_stride_vec4];
+    float4 v = w[0];
+#pragma unroll
+    for (int m = 1; m < kAccWays; ++m) {
+      if (m < nacc) {
+        v.x += w[m].x; v.y += w[m].y; v.z += w[m].z; v.w += w[m].w;
+      }
     }
     uint2 o;
     o.x = pack_bf16x2(scale * v.x, scale * v.y);
