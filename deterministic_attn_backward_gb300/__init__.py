@@ -25,6 +25,7 @@ STATUS = {0: "DAB_OK", 1: "DAB_ERR_INVALID_ARG", 2: "DAB_ERR_UNSUPPORTED", 3: "D
 DAB_BWD_SKIP_PREPROCESS = 0x1
 DAB_BWD_SKIP_CONVERT = 0x2
 DAB_BWD_SKIP_MAIN = 0x4
+DAB_BWD_PLAIN_ADD = 0x8
 
 EXPORTED = (
     "dab_attn_fwd", "dab_bwd_workspace_size", "dab_attn_bwd", "dab_check_status",

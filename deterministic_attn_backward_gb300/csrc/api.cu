@@ -345,6 +345,7 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
   p.scale = scale;
   p.scale_log2e = scale * 1.4426950408889634f;
   p.timeout_ns = timeout;
+  p.plain_add = (flags & DAB_BWD_PLAIN_ADD) ? 1 : 0;
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));

@@ -556,6 +556,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           if (store) {
 #pragma unroll
             for (int q = 0; q < 64; ++q) base[(size_t)q * HD] = __uint_as_float(v[q]);
+          } else if (deterministic && p.plain_add) {
+            // load + add + store, the same IEEE adds in the same order as
+            // the red (only this contributor touches the sub-tile now)
+            fence_acq_rel_gpu();
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+              float a[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) a[k] = ld_cg_f32(base + (size_t)(c + k) * HD);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) base[(size_t)(c + k) * HD] = a[k] + __uint_as_float(v[c + k]);
+            }
           } else {
 #pragma unroll
             for (int q = 0; q < 64; ++q) {
@@ -571,10 +583,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           for (int m = 0; m < 8; ++m) {
             const float a0 = __uint_as_float(v[4 * m]), a1 = __uint_as_float(v[4 * m + 1]);
             const float a2 = __uint_as_float(v[4 * m + 2]), a3 = __uint_as_float(v[4 * m + 3]);
-            if (store)
+            if (store) {
               reinterpret_cast<float4*>(base)[m] = make_float4(a0, a1, a2, a3);
-            else
+            } else if (deterministic && p.plain_add) {
+              if (m == 0) fence_acq_rel_gpu();
+              const float4 b = ld_cg_v4_f32(base + 4 * m);
+              reinterpret_cast<float4*>(base)[m] = make_float4(b.x + a0, b.y + a1, b.z + a2, b.w + a3);
+            } else {
               red_add_v4_f32(base + 4 * m, a0, a1, a2, a3);
+            }
           }
         }
         if (deterministic) {

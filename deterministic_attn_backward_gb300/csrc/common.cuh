@@ -56,6 +56,7 @@ struct BwdParams {
   int units_per_head, total_units;
   float scale, scale_log2e;
   unsigned long long timeout_ns;
+  int plain_add;                        // ordered schedules: load + add + store instead of red
 };
 
 struct FwdParams {

@@ -164,6 +164,10 @@ typedef struct {
  * runs the convert kernel alone, so that its time can be taken; dQ, dK and
  * dV are then not the gradients).                                          */
 #define DAB_BWD_SKIP_MAIN 0x4u
+/* Ordered schedules: add each dQ partial to the accumulator with a load from
+ * the L2, an add in registers and a store, instead of red.add.f32 in the L2
+ * (the same additions in the same order; the default is the red).          */
+#define DAB_BWD_PLAIN_ADD 0x8u
 
 dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v,
                              const void* o, const float* lse, const void* dout,

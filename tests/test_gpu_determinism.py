@@ -60,3 +60,21 @@ def test_auto_runs_the_selected_schedule(shape, mask):
     for run in auto:
         for a, b in zip(run, named):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ["full", "causal"])
+@pytest.mark.parametrize("sched", ["serial", "descending_q", "shift"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_plain_adds_give_the_red_bits(mask, sched, d):
+    """The ordered reduction adds each partial with red.add.f32 in the L2.
+    Done instead as load + add + store (DAB_BWD_PLAIN_ADD), the same IEEE
+    additions in the same order: the same bits."""
+    B, H, S = 2, 4, 1024
+    q, k, v, do = (t.cuda() for t in case(B, H, S, d, 13))
+    o, lse = dab.attn_fwd(q, k, v, mask)
+    red = dab.attn_bwd(q, k, v, o, lse, do, mask, sched)
+    plain = dab.attn_bwd(q, k, v, o, lse, do, mask, sched,
+                         opts=dab.BwdOpts(spin_timeout_ns=0, flags=dab.DAB_BWD_PLAIN_ADD, grid=0))
+    for a, b in zip(red, plain):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
