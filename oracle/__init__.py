@@ -60,6 +60,10 @@ def _declare(lib):
     lib.oracle_attn_bwd_given.argtypes = (
         [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int]
         + [dp] * 6 + [dp] * 6 + [ctypes.c_int])
+    lib.oracle_attn_fwd_bwd_block.restype = ctypes.c_int
+    lib.oracle_attn_fwd_bwd_block.argtypes = (
+        [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_void_p]
+        + [dp] * 4 + [dp] * 6 + [ctypes.c_int])
     ip = ctypes.POINTER(ctypes.c_int)
     lib.oracle_attn_rows.restype = ctypes.c_int
     lib.oracle_attn_rows.argtypes = (
@@ -87,10 +91,12 @@ def default_threads() -> int:
     return max(1, os.cpu_count() or 1)
 
 
-def attn_fwd_bwd(q, k, v, dout, scale: float, causal: bool,
+def attn_fwd_bwd(q, k, v, dout, scale: float, causal: bool, tiles=None,
                  nthreads: int | None = None, lib=None) -> dict:
     """Forward + backward for inputs of shape [..., S, d] (leading dims = heads).
 
+    `tiles`: optional block mask, [S/128][S/128] of 0/1 (row = query tile,
+    column = key tile, 0 = masked), combined with `causal`.
     Returns a dict of float64 arrays: o, lse, D, dq, dk, dv.
     """
     lib = lib or load()
@@ -101,12 +107,16 @@ def attn_fwd_bwd(q, k, v, dout, scale: float, causal: bool,
     out = {n: np.empty(shape, np.float64) for n in ("o", "dq", "dk", "dv")}
     out["lse"] = np.empty(shape[:-1], np.float64)
     out["D"] = np.empty(shape[:-1], np.float64)
-    rc = lib.oracle_attn_fwd_bwd(
-        BH, S, d, float(scale), int(bool(causal)),
-        _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
-        _ptr(out["o"]), _ptr(out["lse"]), _ptr(out["D"]),
-        _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
-        int(nthreads or default_threads()))
+    tail = (_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(out["o"]), _ptr(out["lse"]), _ptr(out["D"]),
+            _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), int(nthreads or default_threads()))
+    if tiles is None:
+        rc = lib.oracle_attn_fwd_bwd(BH, S, d, float(scale), int(bool(causal)), *tail)
+    else:
+        t = np.ascontiguousarray(np.asarray(tiles) != 0, dtype=np.uint8)
+        if t.shape != (S // 128, S // 128) or S % 128:
+            raise ValueError("tiles must be [S/128][S/128]")
+        rc = lib.oracle_attn_fwd_bwd_block(BH, S, d, float(scale), int(bool(causal)),
+                                           t.ctypes.data_as(ctypes.c_void_p), *tail)
     if rc != 0:
         raise RuntimeError(f"oracle_attn_fwd_bwd failed ({rc})")
     return out

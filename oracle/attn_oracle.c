@@ -29,7 +29,13 @@
  *
  * Masks: FULL (nothing masked) or CAUSAL (key c masked for query r when
  * c > r; query and key sequences have the same length, so the diagonal is
- * kept and no row is empty).
+ * kept and no row is empty).  Either can be combined with a block mask: a
+ * table of N x N flags over 128 x 128 tiles (row = query tile, column = key
+ * tile), where a zero flag masks every key of that key tile for every query
+ * of that query tile (the block-sparse masks the DASH pages name as future
+ * work, technical summary section 5).  A query row with every key masked
+ * has no softmax: its LSE is -infinity, its O, D and dQ are zero, and it
+ * adds nothing to dK and dV.
  *
  * Organisation: steps 1-6 and 8-10 are computed per query row r (everything
  * they need lives in row r); steps 7 and 11 are sums over query rows for one
@@ -47,8 +53,12 @@
 #include <stdlib.h>
 #include <string.h>
 
+#define BLOCK_TILE 128 /* rows per tile of a block mask */
+
 typedef struct {
     int S, d, causal;
+    const unsigned char *tiles; /* block mask [N][N] (N = S / BLOCK_TILE), or NULL */
+    int ntiles;
     double scale;
     const double *q, *k, *v, *dout; /* [S][d] each, this head */
     const double *o_in, *lse_in;    /* diagnostic mode: given O [S][d], LSE [S] */
@@ -64,7 +74,11 @@ typedef struct {
     int nrows;
 } worker_arg;
 
-static int is_masked(int causal, int r, int c) { return causal && c > r; }
+static int is_masked(const head_job *h, int r, int c)
+{
+    if (h->causal && c > r) return 1;
+    return h->tiles != NULL && h->tiles[(size_t)(r / BLOCK_TILE) * h->ntiles + c / BLOCK_TILE] == 0;
+}
 
 static double dot(const double *a, const double *b, int d)
 {
@@ -86,7 +100,7 @@ static void query_row(const head_job *h, int r, double *s, double *p)
         /* 1. scores of the unmasked keys */
         double m = -INFINITY;
         for (int c = 0; c < S; ++c) {
-            if (is_masked(h->causal, r, c)) continue;
+            if (is_masked(h, r, c)) continue;
             s[c] = h->scale * dot(q_r, h->k + (size_t)c * d, d);
             /* 2. running maximum */
             if (s[c] > m) m = s[c];
@@ -94,11 +108,11 @@ static void query_row(const head_job *h, int r, double *s, double *p)
         /* 3. log-sum-exp */
         double sum = 0.0;
         for (int c = 0; c < S; ++c)
-            if (!is_masked(h->causal, r, c)) sum += exp(s[c] - m);
-        lse = m + log(sum);
+            if (!is_masked(h, r, c)) sum += exp(s[c] - m);
+        lse = (sum > 0.0) ? m + log(sum) : -INFINITY; /* no visible key: no softmax */
         /* 4. probabilities */
         for (int c = 0; c < S; ++c)
-            p[c] = is_masked(h->causal, r, c) ? 0.0 : exp(s[c] - lse);
+            p[c] = is_masked(h, r, c) ? 0.0 : exp(s[c] - lse);
         /* 5. output row */
         for (int x = 0; x < d; ++x) o_r[x] = 0.0;
         for (int c = 0; c < S; ++c) {
@@ -110,7 +124,7 @@ static void query_row(const head_job *h, int r, double *s, double *p)
         /* diagnostic mode: O and LSE given; P from the given LSE */
         lse = h->lse_in[r];
         for (int c = 0; c < S; ++c)
-            p[c] = is_masked(h->causal, r, c)
+            p[c] = is_masked(h, r, c)
                        ? 0.0
                        : exp(h->scale * dot(q_r, h->k + (size_t)c * d, d) - lse);
         memcpy(o_r, h->o_in + (size_t)r * d, sizeof(double) * (size_t)d);
@@ -125,7 +139,7 @@ static void query_row(const head_job *h, int r, double *s, double *p)
     double *dq_r = h->dq + (size_t)r * d;
     for (int x = 0; x < d; ++x) dq_r[x] = 0.0;
     for (int c = 0; c < S; ++c) {
-        if (is_masked(h->causal, r, c)) continue;
+        if (is_masked(h, r, c)) continue;
         const double dp = dot(do_r, h->v + (size_t)c * d, d); /* 8 */
         const double ds = p[c] * (dp - D);                    /* 9 */
         const double *k_c = h->k + (size_t)c * d;
@@ -144,7 +158,7 @@ static void key_row(const head_job *h, int c)
     double *dv_c = h->dv + (size_t)c * d;
     for (int x = 0; x < d; ++x) { dk_c[x] = 0.0; dv_c[x] = 0.0; }
     for (int r = 0; r < S; ++r) {
-        if (is_masked(h->causal, r, c)) continue;
+        if (is_masked(h, r, c)) continue;
         const double *q_r = h->q + (size_t)r * d;
         const double *do_r = h->dout + (size_t)r * d;
         const double s = h->scale * dot(q_r, k_c, d);   /* 1 */
@@ -215,16 +229,19 @@ static int run_phase(head_job *h, int phase, int nthreads)
 }
 
 static int run_heads(int BH, int S, int d, double scale, int causal,
+                     const unsigned char *tiles,
                      const double *q, const double *k, const double *v,
                      const double *dout, const double *o_in, const double *lse_in,
                      double *o, double *lse, double *D,
                      double *dq, double *dk, double *dv, int nthreads)
 {
     if (BH < 0 || S < 0 || d <= 0) return -2;
+    if (tiles != NULL && (S % BLOCK_TILE) != 0) return -2;
     for (int b = 0; b < BH; ++b) {
         const size_t off = (size_t)b * (size_t)S * (size_t)d;
         head_job h;
         h.S = S; h.d = d; h.causal = causal; h.scale = scale;
+        h.tiles = tiles; h.ntiles = S / BLOCK_TILE;
         h.q = q + off; h.k = k + off; h.v = v + off; h.dout = dout + off;
         h.o_in = o_in ? o_in + off : NULL;
         h.lse_in = lse_in ? lse_in + (size_t)b * S : NULL;
@@ -243,7 +260,21 @@ int oracle_attn_fwd_bwd(int BH, int S, int d, double scale, int causal,
                         double *o, double *lse, double *D,
                         double *dq, double *dk, double *dv, int nthreads)
 {
-    return run_heads(BH, S, d, scale, causal, q, k, v, dout, NULL, NULL,
+    return run_heads(BH, S, d, scale, causal, NULL, q, k, v, dout, NULL, NULL,
+                     o, lse, D, dq, dk, dv, nthreads);
+}
+
+/* The same with a block mask: tiles [N][N], N = S / 128, row = query tile,
+ * column = key tile, zero = masked (combined with `causal`).               */
+int oracle_attn_fwd_bwd_block(int BH, int S, int d, double scale, int causal,
+                              const unsigned char *tiles,
+                              const double *q, const double *k, const double *v,
+                              const double *dout,
+                              double *o, double *lse, double *D,
+                              double *dq, double *dk, double *dv, int nthreads)
+{
+    if (tiles == NULL) return -2;
+    return run_heads(BH, S, d, scale, causal, tiles, q, k, v, dout, NULL, NULL,
                      o, lse, D, dq, dk, dv, nthreads);
 }
 
@@ -258,7 +289,7 @@ int oracle_attn_bwd_given(int BH, int S, int d, double scale, int causal,
                           double *dq, double *dk, double *dv, int nthreads)
 {
     if (o_in == NULL || lse_in == NULL) return -2;
-    return run_heads(BH, S, d, scale, causal, q, k, v, dout, o_in, lse_in,
+    return run_heads(BH, S, d, scale, causal, NULL, q, k, v, dout, o_in, lse_in,
                      o_out, lse_out, D, dq, dk, dv, nthreads);
 }
 
@@ -289,6 +320,7 @@ int oracle_attn_rows(int S, int d, double scale, int causal,
     head_job h;
     if (!o || !dq || !dk || !dv || !lse || !D) { rc = -1; goto done; }
     h.S = S; h.d = d; h.causal = causal; h.scale = scale;
+    h.tiles = NULL; h.ntiles = 0;
     h.q = q; h.k = k; h.v = v; h.dout = dout;
     h.o_in = NULL; h.lse_in = NULL;
     h.o = o; h.lse = lse; h.D = D; h.dq = dq; h.dk = dk; h.dv = dv;

@@ -209,5 +209,74 @@ def pin_autograd(lib, tol=1e-10):
             assert _relerr(out[n], t.grad.numpy()) < tol, f"autograd {n} causal={causal}"
 
 
+def _run_tiles(lib, q, k, v, do, scale, causal, tiles):
+    return oracle.attn_fwd_bwd(q, k, v, do, scale, causal, tiles=tiles, nthreads=2, lib=lib)
+
+
+def pin_block_autograd(lib, tol=1e-10):
+    """Block masks: torch autograd (float64) with the element mask spelled
+    out from an asymmetric tile table (every row keeps a visible key)."""
+    import torch
+    rng = np.random.default_rng(7)
+    S, d, scale = 384, 6, 0.4
+    for causal, tiles in ((False, [[0, 1, 0], [1, 0, 1], [1, 1, 0]]),
+                          (True, [[1, 0, 0], [1, 1, 0], [0, 1, 1]])):
+        t = np.array(tiles, dtype=np.uint8)
+        q, k, v, do = (_rand(rng, 1, S, d) for _ in range(4))
+        r = np.arange(S)
+        vis = t[r[:, None] // 128, r[None, :] // 128].astype(bool)
+        if causal:
+            vis &= r[None, :] <= r[:, None]
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        sc = (scale * tq @ tk.transpose(-1, -2)).masked_fill(torch.tensor(~vis), float("-inf"))
+        o = torch.softmax(sc, dim=-1) @ tv
+        (o * torch.tensor(do)).sum().backward()
+        out = _run_tiles(lib, q, k, v, do, scale, causal, t)
+        assert _relerr(out["o"], o.detach().numpy()) < tol, f"block o causal={causal}"
+        assert _relerr(out["lse"], torch.logsumexp(sc, -1).detach().numpy()) < tol
+        for n, g in (("dq", tq), ("dk", tk), ("dv", tv)):
+            assert _relerr(out[n], g.grad.numpy()) < tol, f"block autograd {n} causal={causal}"
+
+
+def pin_block_documents(lib, tol=1e-13):
+    """A block-diagonal table (documents of whole tiles) is independent
+    attention on each document: the same as the unmasked oracle run on each
+    document's rows alone."""
+    rng = np.random.default_rng(8)
+    S, d, scale = 512, 5, 0.6
+    docs = ((0, 1), (1, 3), (3, 4))          # tile ranges
+    t = np.zeros((4, 4), np.uint8)
+    for a, b in docs:
+        t[a:b, a:b] = 1
+    q, k, v, do = (_rand(rng, 2, S, d) for _ in range(4))
+    for causal in (False, True):
+        whole = _run_tiles(lib, q, k, v, do, scale, causal, t)
+        for a, b in docs:
+            sl = slice(128 * a, 128 * b)
+            part = _run(lib, q[:, sl], k[:, sl], v[:, sl], do[:, sl], scale, causal)
+            for n in ("o", "lse", "dq", "dk", "dv"):
+                assert _relerr(whole[n][:, sl], part[n]) < tol, f"document {a}-{b} {n} causal={causal}"
+
+
+def pin_block_empty_tiles(lib, tol=1e-13):
+    """A query tile with every key masked has no softmax (LSE -inf, O, D, dQ
+    zero); a key tile nobody sees gets zero dK and dV; the rest is the
+    unmasked problem with that tile's rows and keys removed."""
+    rng = np.random.default_rng(9)
+    S, d, scale = 384, 4, 0.8
+    t = np.array([[1, 0, 1], [0, 0, 0], [1, 0, 1]], np.uint8)
+    q, k, v, do = (_rand(rng, 1, S, d) for _ in range(4))
+    out = _run_tiles(lib, q, k, v, do, scale, False, t)
+    mid = slice(128, 256)
+    assert np.all(np.isneginf(out["lse"][:, mid]))
+    for n in ("o", "D", "dq", "dk", "dv"):
+        assert np.all(out[n][:, mid] == 0.0), f"empty tile {n}"
+    keep = np.r_[0:128, 256:384]
+    rest = _run(lib, q[:, keep], k[:, keep], v[:, keep], do[:, keep], scale, False)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        assert _relerr(out[n][:, keep], rest[n]) < tol, f"empty tiles: rest {n}"
+
+
 ALL_PINS = (pin_finite_differences, pin_worked_example, pin_closed_forms,
-            pin_invariants, pin_autograd)
+            pin_invariants, pin_autograd, pin_block_autograd, pin_block_documents,
+            pin_block_empty_tiles)

@@ -20,16 +20,20 @@ MUTATIONS = [
     ("drop scale on dK", "dk_c[x] *= h->scale;", ";", 0),
     ("sign of D in dS", "const double ds = p[c] * (dp - D);", "const double ds = p[c] * (dp + D);", 0),
     ("D forgotten in dK pass", "const double ds = p * (dp - h->D[r]);", "const double ds = p * dp;", 0),
-    ("causal keeps future key", "return causal && c > r;", "return causal && c > r + 1;", 0),
-    ("causal drops diagonal", "return causal && c > r;", "return causal && c >= r && r > 0;", 0),
-    ("log base 2 for LSE", "lse = m + log(sum);", "lse = m + log2(sum);", 0),
+    ("causal keeps future key", "if (h->causal && c > r) return 1;", "if (h->causal && c > r + 1) return 1;", 0),
+    ("causal drops diagonal", "if (h->causal && c > r) return 1;", "if (h->causal && c >= r && r > 0) return 1;", 0),
+    ("log base 2 for LSE", "m + log(sum)", "m + log2(sum)", 0),
     ("dV uses Q", "dv_c[x] += p * do_r[x];", "dv_c[x] += p * q_r[x];", 0),
     ("dK uses K", "dk_c[x] += ds * q_r[x];", "dk_c[x] += ds * k_c[x];", 0),
     ("dQ uses V", "dq_r[x] += ds * k_c[x];", "dq_r[x] += ds * h->v[(size_t)c * d + x];", 0),
     ("dP transposed (dO.k)", "const double dp = dot(do_r, h->v + (size_t)c * d, d); /* 8 */",
      "const double dp = dot(do_r, h->k + (size_t)c * d, d); /* 8 */", 0),
     ("D from dO.dO", "D = dot(do_r, o_r, d);", "D = dot(do_r, do_r, d);", 0),
-    ("masked keys in dK/dV pass", "if (is_masked(h->causal, r, c)) continue;", ";", 2),
+    ("masked keys in dK/dV pass", "if (is_masked(h, r, c)) continue;", ";", 2),
+    ("block table transposed", "h->tiles[(size_t)(r / BLOCK_TILE) * h->ntiles + c / BLOCK_TILE]",
+     "h->tiles[(size_t)(c / BLOCK_TILE) * h->ntiles + r / BLOCK_TILE]", 0),
+    ("block mask ignored", "return h->tiles != NULL && ", "return 0 && h->tiles != NULL && ", 0),
+    ("empty row gets LSE 0", ": -INFINITY; /* no visible key", ": 0.0; /* no visible key", 0),
     ("no scale in scores", "s[c] = h->scale * dot(q_r, h->k + (size_t)c * d, d);",
      "s[c] = dot(q_r, h->k + (size_t)c * d, d);", 0),
 ]
