@@ -383,6 +383,67 @@ SWEEP_CONFIGS = [
      for d_ in (64, 128) for s_ in (1024, 2048, 4096, 8192, 16384, 32768)]
 
 
+# Block-mask configurations (tile flags over 128 x 128 tiles): a sliding
+# window of `w` tiles before the query (causal), and documents of `w` tiles
+# (block diagonal, causal inside a document).  FLOPs count the visible tiles
+# (10 * 128^2 * d each; a causal diagonal tile counts half).
+BLOCK_CONFIGS = [
+    ("BM-window-1k", 2, 16, 8192, 128, 2, 0.5, "window", 8),
+    ("BM-docs-2k", 2, 16, 8192, 128, 2, 0.5, "docs", 16),
+    ("BM-docs-8k", 1, 16, 32768, 128, 4, 1.0, "docs", 64),
+]
+
+
+def block_tiles(kind: str, N: int, w: int):
+    import numpy as np
+    j, i = np.meshgrid(np.arange(N), np.arange(N), indexing="ij")   # j: query tile, i: key tile
+    if kind == "window":
+        return ((i <= j) & (j - i < w)).astype(np.uint8)
+    return (j // w == i // w).astype(np.uint8)
+
+
+def run_block_sweep(reps: int) -> None:
+    """Block masks: every schedule that supports them, one JSON line per config."""
+    import numpy as np
+    import torch
+    import deterministic_attn_backward_gb300 as dab
+    from deterministic_attn_backward_gb300 import inputs
+    dab.load_library()
+    peak = load_peaks()["bf16_tflops"]
+    stream = torch.cuda.current_stream()
+    for name, b, h, s_, d, seed, qks, kind, w in BLOCK_CONFIGS:
+        N = s_ // 128
+        t = block_tiles(kind, N, w)
+        jj, ii = np.meshgrid(np.arange(N), np.arange(N), indexing="ij")
+        vis = (t.astype(bool) & (ii <= jj)).astype(np.float64)           # the causal mask applies too
+        vis[np.arange(N), np.arange(N)] *= 0.5                            # causal diagonal tiles
+        fl = float(vis.sum()) * 10.0 * 128 * 128 * d * b * h
+        q, k, v, do = (x.cuda() for x in inputs.make_qkvdo(b, h, s_, d, seed, qks))
+        o, lse = dab.attn_fwd(q, k, v, "causal", tiles=t)
+        ws = dab.new_workspace(b, h, s_, d, sched="serial", block=True)
+        out = tuple(torch.empty_like(q) for _ in range(3))
+        row = {"config": name, "B": b, "H": h, "S": s_, "d": d, "mask": f"causal+{kind}{w}",
+               "visible_tiles": float(vis.sum()), "scheds": {}}
+        for sched in ("serial", "descending_q", "atomic"):
+            ts = []
+            for it in range(3 + reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                dab.attn_bwd(q, k, v, o, lse, do, "causal", sched, workspace=ws, out=out, tiles=t)
+                e1.record(stream)
+                e1.synchronize()
+                if it >= 3:
+                    ts.append(e0.elapsed_time(e1))
+            ms = statistics.median(ts)
+            tf = fl / (ms * 1e-3) / 1e12
+            row["scheds"][sched] = {"ms": round(ms, 4), "tflops": round(tf, 1),
+                                    "frac": round(tf / peak, 4), "status": dab.check_status(ws)}
+        print(json.dumps(row), flush=True)
+        del q, k, v, do, ws, out
+        torch.cuda.empty_cache()
+
+
 def run_sweep(which: str, reps: int) -> None:
     """Every schedule on every measurement configuration: per (config, mask)
     one JSON line with ms, TFLOP/s, fraction of the measured peak and the gap
@@ -544,10 +605,16 @@ def main():
     ap.add_argument("--case", default=None, help="B,H,S,d,mask,sched: time one configuration")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--sweep", default=None,
-                    help="all | C1 | C2 | C3 | C4: every schedule on the measurement configurations")
+                    help="all | C1 | C2 | C3 | C4 | block: every schedule on the measurement "
+                         "configurations (block: the block-mask ones)")
     args = ap.parse_args()
     if args.sweep:
-        run_sweep(args.sweep, max(args.reps, 5))
+        if args.sweep in ("all", "block"):
+            if args.sweep == "all":
+                run_sweep("all", max(args.reps, 5))
+            run_block_sweep(max(args.reps, 5))
+        else:
+            run_sweep(args.sweep, max(args.reps, 5))
         return
     if args.case:
         for spec in args.case.split(";"):

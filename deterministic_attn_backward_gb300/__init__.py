@@ -33,6 +33,7 @@ EXPORTED = (
     "dab_sched_units_per_head", "dab_sched_unit_steps", "dab_sched_step", "dab_sched_rank",
     "dab_sched_contributors", "dab_sched_gang_size", "dab_dag_simulate", "dab_dag_critical_path",
     "dab_dag_simulate_ways", "dab_sched_select", "dab_attn_bwd_host", "dab_bwd_host_workspace_size",
+    "dab_attn_fwd_block", "dab_attn_bwd_block", "dab_bwd_block_workspace_size",
     "dab_selftest_mma", "dab_last_error_string", "dab_attn_bwd_noalloc", "dab_mma_peak",
     "dab_mma_peak_grid",
 )
@@ -111,6 +112,12 @@ def load_library(path: str = LIB_PATH):
     lib.dab_bwd_host_workspace_size.restype = sz
     lib.dab_attn_bwd_host.argtypes = [vp] * 9 + [i] * 4 + [f, i, i, vp, sz, i, vp]
     lib.dab_attn_bwd_host.restype = i
+    lib.dab_attn_fwd_block.argtypes = [vp] * 5 + [i] * 4 + [f, vp, i, vp, sz, vp]
+    lib.dab_attn_fwd_block.restype = i
+    lib.dab_bwd_block_workspace_size.argtypes = [i] * 5
+    lib.dab_bwd_block_workspace_size.restype = sz
+    lib.dab_attn_bwd_block.argtypes = [vp] * 9 + [i] * 4 + [f, vp, i, i, vp, sz, vp]
+    lib.dab_attn_bwd_block.restype = i
     lib.dab_dag_critical_path.argtypes = [i, i, i, ctypes.c_double, ctypes.c_double, i]
     lib.dab_dag_critical_path.restype = ctypes.c_double
     lib.dab_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 4 + [f, i, i, vp]
@@ -169,12 +176,29 @@ def workspace_layout(B, H, S, d, mask="full", sched="serial") -> WsLayout:
     return L
 
 
-def new_workspace(B, H, S, d, mask="full", sched="serial", device="cuda") -> torch.Tensor:
-    return torch.empty(workspace_size(B, H, S, d, mask, sched), dtype=torch.uint8, device=device)
+def block_workspace_size(B, H, S, d, sched="descending_q") -> int:
+    n = int(load_library().dab_bwd_block_workspace_size(B, H, S, d, _sched(sched)))
+    if n == 0:
+        raise DabError(1, "dab_bwd_block_workspace_size")
+    return n
 
 
-def attn_fwd(q, k, v, mask="full", scale=None, workspace=None, out=None, lse=None):
-    """O (bf16 [B,H,S,d]) and LSE (f32 [B,H,S]) on q's CUDA device."""
+def new_workspace(B, H, S, d, mask="full", sched="serial", device="cuda", block=False) -> torch.Tensor:
+    n = block_workspace_size(B, H, S, d, sched) if block else workspace_size(B, H, S, d, mask, sched)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _tiles(tiles, S, dev):
+    """Block mask as a contiguous uint8 [S/128, S/128] CUDA tensor."""
+    t = torch.as_tensor(tiles)
+    if tuple(t.shape) != (S // 128, S // 128):
+        raise ValueError("tiles must be [S/128, S/128]")
+    return (t != 0).to(device=dev, dtype=torch.uint8).contiguous()
+
+
+def attn_fwd(q, k, v, mask="full", scale=None, workspace=None, out=None, lse=None, tiles=None):
+    """O (bf16 [B,H,S,d]) and LSE (f32 [B,H,S]) on q's CUDA device.
+    `tiles`: optional block mask [S/128, S/128] (dab_attn_fwd_block)."""
     lib = load_library()
     B, H, S, d = _shape(q)
     dev = q.device if q.is_cuda else torch.device("cuda")
@@ -182,10 +206,16 @@ def attn_fwd(q, k, v, mask="full", scale=None, workspace=None, out=None, lse=Non
     o = out if out is not None else torch.empty_like(q)
     lse_t = lse if lse is not None else torch.empty((B, H, S), dtype=torch.float32, device=dev)
     ws_ptr, ws_n = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
-    _check(lib.dab_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                            lse_t.data_ptr(), B, H, S, d,
-                            float(scale if scale is not None else default_scale(d)),
-                            _mask(mask), ws_ptr, ws_n, _stream(dev)), "dab_attn_fwd")
+    sc = float(scale if scale is not None else default_scale(d))
+    if tiles is None:
+        _check(lib.dab_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse_t.data_ptr(), B, H, S, d, sc, _mask(mask), ws_ptr, ws_n,
+                                _stream(dev)), "dab_attn_fwd")
+    else:
+        t = _tiles(tiles, S, dev)
+        _check(lib.dab_attn_fwd_block(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      lse_t.data_ptr(), B, H, S, d, sc, t.data_ptr(), _mask(mask),
+                                      ws_ptr, ws_n, _stream(dev)), "dab_attn_fwd_block")
     return o, lse_t
 
 
@@ -229,7 +259,7 @@ def _attn_bwd_host(q, k, v, o, lse, dout, mask, sched, scale, workspace, out, ch
 
 
 def attn_bwd(q, k, v, o, lse, dout, mask="full", sched="serial", scale=None, workspace=None,
-             out=None, opts: BwdOpts | None = None, chunks: int = 0):
+             out=None, opts: BwdOpts | None = None, chunks: int = 0, tiles=None):
     """dQ, dK, dV (bf16 [B,H,S,d]) through the C ABI.
 
     Device tensors are used in place (dab_attn_bwd / dab_attn_bwd_ex).  CPU
@@ -241,6 +271,8 @@ def attn_bwd(q, k, v, o, lse, dout, mask="full", sched="serial", scale=None, wor
     lib = load_library()
     B, H, S, d = _shape(q)
     host = not q.is_cuda
+    if tiles is not None:
+        return _attn_bwd_block(q, k, v, o, lse, dout, mask, sched, scale, workspace, out, tiles)
     if host:
         if opts is not None:
             raise ValueError("opts apply to device tensors only")
@@ -263,6 +295,26 @@ def attn_bwd(q, k, v, o, lse, dout, mask="full", sched="serial", scale=None, wor
         _check(lib.dab_attn_bwd(*args), "dab_attn_bwd")
     else:
         _check(lib.dab_attn_bwd_ex(*args, ctypes.byref(opts)), "dab_attn_bwd_ex")
+    return dq, dk, dv
+
+
+def _attn_bwd_block(q, k, v, o, lse, dout, mask, sched, scale, workspace, out, tiles):
+    """dab_attn_bwd_block on CUDA tensors (mask: "full" or "causal")."""
+    lib = load_library()
+    B, H, S, d = _shape(q)
+    dev = q.device
+    q, k, v, o, dout = (_dev_bf16(t, dev) for t in (q, k, v, o, dout))
+    t = _tiles(tiles, S, dev)
+    if workspace is None:
+        workspace = new_workspace(B, H, S, d, sched=sched, device=dev, block=True)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(q), torch.empty_like(q))
+    dq, dk, dv = out
+    _check(lib.dab_attn_bwd_block(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                  dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, d,
+                                  float(scale if scale is not None else default_scale(d)), t.data_ptr(),
+                                  _mask(mask), _sched(sched), workspace.data_ptr(), workspace.numel(),
+                                  _stream(dev)), "dab_attn_bwd_block")
     return dq, dk, dv
 
 

@@ -31,7 +31,10 @@ cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const flo
                               long long dq_elems, int rows, int grid, cudaStream_t stream);
 cudaError_t launch_convert(const float* dqacc, void* dq, long long elems, float scale,
                            long long acc_stride, int ways, int causal, int N, int S, int d, int grid,
-                           cudaStream_t stream);
+                           const int* count, cudaStream_t stream);
+cudaError_t launch_block_tables(const uint8_t* tiles, int N, int causal, int descending,
+                                uint16_t* list, uint16_t* rank, int* nact, int* count,
+                                cudaStream_t stream);
 }  // namespace dab
 
 namespace {
@@ -181,6 +184,21 @@ bool layout(int B, int H, int S, int d, dab_sched_t sched, dab_ws_layout_t* L) {
   return true;
 }
 
+// Block-mask schedule tables, after the ordinary workspace regions.
+struct BlockTables {
+  size_t list, rank, nact, count, total;
+};
+BlockTables block_tables_layout(const dab_ws_layout_t& L, int N) {
+  BlockTables T;
+  const size_t n2 = (size_t)N * N;
+  T.list = round_up(L.total, 256);
+  T.rank = T.list + 2 * n2;
+  T.nact = round_up(T.rank + 2 * n2, 16);
+  T.count = T.nact + 4 * (size_t)N;
+  T.total = round_up(T.count + 4 * (size_t)N, 256);
+  return T;
+}
+
 int elementwise_grid(int sms, long long work) {
   long long g = (long long)sms * 8;
   const long long need = (work + 255) / 256;
@@ -221,9 +239,9 @@ size_t dab_bwd_workspace_size(int B, int H, int S, int d, dab_mask_t mask, dab_s
   return L.total;
 }
 
-dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                          int H, int S, int d, float scale, dab_mask_t mask, void* workspace,
-                          size_t ws_bytes, cudaStream_t stream) {
+static dab_status_t fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                             int H, int S, int d, float scale, dab_mask_t mask, void* workspace,
+                             size_t ws_bytes, cudaStream_t stream, const uint8_t* tiles) {
   if (check_shape(B, H, S, d) != DAB_OK) return DAB_ERR_INVALID_ARG;
   if ((int)mask < 0 || (int)mask > 1) return DAB_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -244,6 +262,7 @@ dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v, void* o, 
   p.N = S / 128;
   p.mask = (int)mask;
   p.scale_log2e = scale * 1.4426950408889634f;
+  p.tiles = tiles;
   dab::WsHeader* hdr = static_cast<dab::WsHeader*>(workspace);
   if (hdr != nullptr && cudaMemsetAsync(hdr, 0, 16, stream) != cudaSuccess) return DAB_ERR_CUDA;
   const dim3 grid((unsigned)(p.BH * p.N)), block(192);
@@ -254,6 +273,20 @@ dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v, void* o, 
   else
     e = cudaLaunchKernel(dab::fwd_kernel_ptr<64>(), grid, block, args, dab::fwd_smem_bytes<64>(), stream);
   return e == cudaSuccess ? DAB_OK : cuda_fail(e, "forward launch");
+}
+
+dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                          int H, int S, int d, float scale, dab_mask_t mask, void* workspace,
+                          size_t ws_bytes, cudaStream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, S, d, scale, mask, workspace, ws_bytes, stream, nullptr);
+}
+
+dab_status_t dab_attn_fwd_block(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int S, int d, float scale, const uint8_t* tiles,
+                                int causal, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (tiles == nullptr || (causal != 0 && causal != 1)) return DAB_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, H, S, d, scale, causal ? DAB_MASK_CAUSAL : DAB_MASK_FULL,
+                  workspace, ws_bytes, stream, tiles);
 }
 
 dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dout, int B, int H, int S,
@@ -280,17 +313,22 @@ dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dou
   return e == cudaSuccess ? DAB_OK : cuda_fail(e, "preprocess launch");
 }
 
-dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+// The backward; `tiles` (device, [N][N]) selects the block-mask schedules.
+static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const void* o,
                              const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                              int H, int S, int d, float scale, dab_mask_t mask, dab_sched_t sched,
                              void* workspace, size_t ws_bytes, cudaStream_t stream,
-                             const dab_bwd_opts_t* opts) {
+                             const dab_bwd_opts_t* opts, const uint8_t* tiles) {
   if (check_shape(B, H, S, d) != DAB_OK || check_enums_auto(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return DAB_ERR_INVALID_ARG;
   if (!(scale > 0.f)) return DAB_ERR_INVALID_ARG;
-  {
+  const bool block = tiles != nullptr;
+  if (block) {
+    if (sched == DAB_SCHED_AUTO) sched = DAB_SCHED_DESCENDING_Q;
+    if (sched == DAB_SCHED_SHIFT) return DAB_ERR_UNSUPPORTED;  // no shift walk over a block mask
+  } else {
     const dab_status_t st = resolve_sched(mask, B, H, S, (opts && opts->grid > 0) ? opts->grid : 0, &sched);
     if (st != DAB_OK) return st;
   }
@@ -298,26 +336,35 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
   if (sched == DAB_SCHED_SHIFT && mask == DAB_MASK_CAUSAL && (N % 2) != 0) return DAB_ERR_UNSUPPORTED;
   dab_ws_layout_t L;
   layout(B, H, S, d, sched, &L);
-  if (workspace == nullptr || !aligned16(workspace) || ws_bytes < L.total) return DAB_ERR_WORKSPACE;
+  const BlockTables T = block_tables_layout(L, N);
+  if (workspace == nullptr || !aligned16(workspace) || ws_bytes < (block ? T.total : L.total))
+    return DAB_ERR_WORKSPACE;
   int sms = 0;
   if (!device_setup(nullptr, &sms)) return DAB_ERR_UNSUPPORTED;
 
   const uint32_t flags = opts ? opts->flags : 0u;
   const unsigned long long timeout =
       (opts && opts->spin_timeout_ns) ? (unsigned long long)opts->spin_timeout_ns : kDefaultTimeoutNs;
-  const int uph = dab::units_per_head((int)sched, (int)mask, N);
+  const int uph = block ? N : dab::units_per_head((int)sched, (int)mask, N);
   const long long total_ll = (long long)B * H * uph;
   if (total_ll >= (1ll << 31)) return DAB_ERR_INVALID_ARG;
   const int total = (int)total_ll;
   int grid = (opts && opts->grid > 0) ? opts->grid : sms;
   if (grid > sms) grid = sms;  // one CTA per SM, all resident
   if (grid > total) grid = total;
-  if (dab::gang_size((int)sched, (int)mask, N) > grid) return DAB_ERR_UNSUPPORTED;
+  if (!block && dab::gang_size((int)sched, (int)mask, N) > grid) return DAB_ERR_UNSUPPORTED;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (!(flags & DAB_BWD_SKIP_PREPROCESS)) {
     dab_status_t st = dab_bwd_preprocess(o, lse, dout, B, H, S, d, mask, sched, workspace, ws_bytes, stream);
     if (st != DAB_OK) return st;
+  }
+  if (block) {
+    const cudaError_t e = dab::launch_block_tables(
+        tiles, N, mask == DAB_MASK_CAUSAL ? 1 : 0, sched == DAB_SCHED_DESCENDING_Q ? 1 : 0,
+        reinterpret_cast<uint16_t*>(ws + T.list), reinterpret_cast<uint16_t*>(ws + T.rank),
+        reinterpret_cast<int*>(ws + T.nact), reinterpret_cast<int*>(ws + T.count), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "block table launch");
   }
 
   dab::BwdParams p;
@@ -346,6 +393,13 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
   p.scale_log2e = scale * 1.4426950408889634f;
   p.timeout_ns = timeout;
   p.plain_add = (flags & DAB_BWD_PLAIN_ADD) ? 1 : 0;
+  if (block) {
+    p.block = 1;
+    p.blk_list = reinterpret_cast<const uint16_t*>(ws + T.list);
+    p.blk_rank = reinterpret_cast<const uint16_t*>(ws + T.rank);
+    p.blk_nact = reinterpret_cast<const int*>(ws + T.nact);
+    p.blk_count = reinterpret_cast<const int*>(ws + T.count);
+  }
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
@@ -369,10 +423,38 @@ dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const 
     const long long elems = rows * d;
     e = dab::launch_convert(p.dqacc, dq, elems, scale, p.acc_stride, p.acc_ways,
                             mask == DAB_MASK_CAUSAL ? 1 : 0, N, S, d, elementwise_grid(sms, elems / 4),
-                            stream);
+                            block ? p.blk_count : nullptr, stream);
     if (e != cudaSuccess) return cuda_fail(e, "convert launch");
   }
   return DAB_OK;
+}
+
+dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                             int H, int S, int d, float scale, dab_mask_t mask, dab_sched_t sched,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream,
+                             const dab_bwd_opts_t* opts) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, S, d, scale, mask, sched, workspace, ws_bytes,
+                  stream, opts, nullptr);
+}
+
+size_t dab_bwd_block_workspace_size(int B, int H, int S, int d, dab_sched_t sched) {
+  if (sched == DAB_SCHED_SHIFT) return 0;
+  if (sched == DAB_SCHED_AUTO) sched = DAB_SCHED_DESCENDING_Q;
+  dab_ws_layout_t L;
+  if (check_enums(DAB_MASK_FULL, sched) != DAB_OK || !layout(B, H, S, d, sched, &L)) return 0;
+  return block_tables_layout(L, S / 128).total;
+}
+
+dab_status_t dab_attn_bwd_block(const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                int B, int H, int S, int d, float scale, const uint8_t* tiles,
+                                int causal, dab_sched_t sched, void* workspace, size_t ws_bytes,
+                                cudaStream_t stream) {
+  if (tiles == nullptr || (causal != 0 && causal != 1)) return DAB_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, S, d, scale,
+                  causal ? DAB_MASK_CAUSAL : DAB_MASK_FULL, sched, workspace, ws_bytes, stream, nullptr,
+                  tiles);
 }
 
 dab_status_t dab_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

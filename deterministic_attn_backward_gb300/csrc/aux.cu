@@ -83,16 +83,23 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
 __global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__ acc,
                                                       uint2* __restrict__ out, long long n_vec4,
                                                       float scale, long long acc_stride_vec4,
-                                                      int ways, int causal, int N, int S, int d) {
+                                                      int ways, int causal, int N, int S, int d,
+                                                      const int* __restrict__ count) {
   const long long n = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec4; i += n) {
     // buffers that received a contribution: min(ways, contributors of the Q
-    // tile), with N contributors per tile for the full mask, j + 1 for causal
+    // tile), with N contributors per tile for the full mask, j + 1 for
+    // causal, and the tables' count under a block mask (0: dQ = 0)
     int nacc = ways < N ? ways : N;
-    if (causal && nacc > 1) {
+    if (count != nullptr || (causal && nacc > 1)) {
       const long long row = (i * 4) / d;
       const int j = (int)((row % S) / kTile);
-      if (j + 1 < nacc) nacc = j + 1;
+      const int c = (count != nullptr) ? count[j] : j + 1;
+      if (c < nacc) nacc = c;
+    }
+    if (nacc == 0) {
+      out[i] = make_uint2(0u, 0u);
+      continue;
     }
     // all loads first (at most kAccWays buffers), then the sum in the
     // fixed order buffer 0, 1, ...
@@ -114,7 +121,41 @@ __global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__
   }
 }
 
+// Schedule tables of a block mask (one CTA): for each KV tile i its visible Q
+// tiles in visit order (ascending, or descending for DESCENDING_Q) and their
+// number; for each Q tile j the rank of each visible KV tile in ascending KV
+// order and the number of contributors.  Visible: flag (j, i) set and, for
+// the causal mask, i <= j.
+__global__ void block_tables_kernel(const uint8_t* __restrict__ tiles, int N, int causal,
+                                    int descending, uint16_t* __restrict__ list,
+                                    uint16_t* __restrict__ rank, int* __restrict__ nact,
+                                    int* __restrict__ count) {
+  auto vis = [&](int j, int i) { return tiles[(size_t)j * N + i] != 0 && (!causal || i <= j); };
+  for (int x = threadIdx.x; x < N; x += blockDim.x) {
+    int n = 0;
+    for (int t = 0; t < N; ++t) {
+      const int j = descending ? N - 1 - t : t;
+      if (vis(j, x)) list[(size_t)x * N + n++] = (uint16_t)j;
+    }
+    nact[x] = n;
+    int r = 0;
+    for (int i = 0; i < N; ++i) {
+      const bool v = vis(x, i);
+      rank[(size_t)x * N + i] = v ? (uint16_t)r : (uint16_t)0xFFFFu;
+      r += v ? 1 : 0;
+    }
+    count[x] = r;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_block_tables(const uint8_t* tiles, int N, int causal, int descending,
+                                uint16_t* list, uint16_t* rank, int* nact, int* count,
+                                cudaStream_t stream) {
+  block_tables_kernel<<<1, 256, 0, stream>>>(tiles, N, causal, descending, list, rank, nact, count);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const float* lse, float* D,
                               float* lse2, uint32_t* sem, int n_sem, WsHeader* hdr, float* dqacc,
@@ -135,10 +176,10 @@ cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const flo
 
 cudaError_t launch_convert(const float* dqacc, void* dq, long long elems, float scale,
                            long long acc_stride, int ways, int causal, int N, int S, int d, int grid,
-                           cudaStream_t stream) {
+                           const int* count, cudaStream_t stream) {
   convert_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dqacc),
                                            reinterpret_cast<uint2*>(dq), elems / 4, scale,
-                                           acc_stride / 4, ways, causal, N, S, d);
+                                           acc_stride / 4, ways, causal, N, S, d, count);
   return cudaGetLastError();
 }
 

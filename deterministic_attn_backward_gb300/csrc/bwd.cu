@@ -111,6 +111,27 @@ static __device__ __noinline__ bool sem_wait(const uint32_t* sem, uint32_t targe
   }
 }
 
+// Schedule of unit u (one KV tile's chain, or a causal shift pair): the
+// fixed schedules of tile_sched.h, or under a block mask the tables built
+// from the tile flags (the KV tile's visible Q tiles in visit order; ranks in
+// ascending KV order, shared by serial and descending as without a mask).
+__device__ __forceinline__ int k_unit_steps(const BwdParams& p, int u) {
+  return p.block ? p.blk_nact[u] : unit_steps(p.sched, p.mask, p.N, u);
+}
+__device__ __forceinline__ Step k_step(const BwdParams& p, int u, int t, int steps) {
+  if (!p.block) return step(p.sched, p.mask, p.N, u, t);
+  Step s;
+  s.kv = u;
+  s.q = p.blk_list[(size_t)u * p.N + t];
+  s.chain_first = (t == 0);
+  s.chain_last = (t == steps - 1);
+  return s;
+}
+__device__ __forceinline__ int k_rank(const BwdParams& p, int i, int j) {
+  if (!p.block) return rank(p.sched, p.mask, p.N, i, j);
+  return p.sched == kSchedAtomic ? -1 : (int)p.blk_rank[(size_t)j * p.N + i];
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = Cfg<HD>;
@@ -190,9 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         ++uidx;
         if (U < 0) break;
         const int bh = U / p.units_per_head, u = U % p.units_per_head;
-        const int steps = unit_steps(p.sched, p.mask, p.N, u);
+        const int steps = k_unit_steps(p, u);
         for (int t = 0; t < steps; ++t) {
-          const Step st = step(p.sched, p.mask, p.N, u, t);
+          const Step st = k_step(p, u, t, steps);
           if (st.chain_first) {
             if (chain > 0 && !mbar_wait(&bars->kv_empty, (chain - 1) & 1, wc, 2)) { ok = false; break; }
             mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
@@ -275,9 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         ++uidx;
         if (U < 0) break;
         const int u = U % p.units_per_head;
-        const int steps = unit_steps(p.sched, p.mask, p.N, u);
+        const int steps = k_unit_steps(p, u);
         for (int t = 0; t < steps; ++t) {
-          const Step st = step(p.sched, p.mask, p.N, u, t);
+          const Step st = k_step(p, u, t, steps);
           const int stage = s & 1;
           if (!pre) {
             if (st.chain_first && !mbar_wait(&bars->kv_full, chain & 1, wc, 11)) { ok = false; break; }
@@ -370,9 +391,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       ++uidx;
       if (U < 0) break;
       const int bh = U / p.units_per_head, u = U % p.units_per_head;
-      const int steps = unit_steps(p.sched, p.mask, p.N, u);
+      const int steps = k_unit_steps(p, u);
+      if (steps == 0) {
+        // A KV tile that no visible Q tile meets (block mask): dK = dV = 0.
+        const size_t row = (size_t)bh * p.S + (size_t)u * kTile + r;
+        uint4* dst = reinterpret_cast<uint4*>((h == 0 ? p.dv : p.dk) + row * HD);
+#pragma unroll
+        for (int c = 0; c < HD / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
       for (int t = 0; t < steps; ++t) {
-        const Step st = step(p.sched, p.mask, p.N, u, t);
+        const Step st = k_step(p, u, t, steps);
         const int stage = s & 1;
         const float* lse = s_lse + stage * 128 + 64 * h;
         const float* dd = s_dd + stage * 128 + 64 * h;
@@ -515,12 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       ++uidx;
       if (U < 0) break;
       const int bh = U / p.units_per_head, u = U % p.units_per_head;
-      const int steps = unit_steps(p.sched, p.mask, p.N, u);
+      const int steps = k_unit_steps(p, u);
       for (int t = 0; t < steps; ++t) {
-        const Step st = step(p.sched, p.mask, p.N, u, t);
+        const Step st = k_step(p, u, t, steps);
         // everything but the values is computed before the drain
         // rank r -> buffer r mod ways, position r / ways within that buffer
-        const int rank = deterministic ? dab::rank(p.sched, p.mask, p.N, st.kv, st.q) : 0;
+        const int rank = deterministic ? k_rank(p, st.kv, st.q) : 0;
         const int way = rank % p.acc_ways, lrank = rank / p.acc_ways;
         const size_t sem_idx = (((size_t)bh * p.N + st.q) * kSubTiles + sub) * p.acc_ways + way;
         uint32_t* sem = p.sem + sem_idx;

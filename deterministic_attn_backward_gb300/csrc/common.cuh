@@ -57,6 +57,13 @@ struct BwdParams {
   float scale, scale_log2e;
   unsigned long long timeout_ns;
   int plain_add;                        // ordered schedules: load + add + store instead of red
+  // Block mask (block != 0): the schedule comes from tables built on the
+  // device from the tile flags, shared by all heads.
+  int block;
+  const uint16_t* blk_list;             // [N][N]: KV tile i's visible Q tiles, visit order
+  const uint16_t* blk_rank;             // [N][N]: rank of KV tile i in dQ_j's order, at [j][i]
+  const int* blk_nact;                  // [N]: visible Q tiles of KV tile i
+  const int* blk_count;                 // [N]: contributors of Q tile j
 };
 
 struct FwdParams {
@@ -66,6 +73,7 @@ struct FwdParams {
   int BH, S, N;
   int mask;
   float scale_log2e;
+  const uint8_t* tiles;                 // block mask [N][N] (query tile, key tile), or null
 };
 
 // Record the first device error (later ones are dropped).

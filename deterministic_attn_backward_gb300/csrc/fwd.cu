@@ -8,6 +8,8 @@
 //           to tensor memory, O += P V_c on the tensor cores.
 // Recomputing S once avoids rescaling the O accumulator; this kernel only
 // prepares the backward's inputs, so simplicity wins over its speed.
+// With a block mask, KV tiles whose flag is zero are skipped by every role;
+// a Q tile with no visible KV tile gets O = 0 and LSE = -infinity.
 // Warps: 0 TMA producer, 1 MMA issuer, 2-5 softmax (thread = Q row).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -66,6 +68,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   }
   const int bh = blockIdx.x / p.N, qi = blockIdx.x % p.N;
   const int nkv = (p.mask == kMaskCausal) ? qi + 1 : p.N;
+  // KV tile c takes part unless the block mask hides it (uniform per CTA)
+  auto visible = [&](int c) { return p.tiles == nullptr || p.tiles[(size_t)qi * p.N + c] != 0; };
   const unsigned long long timeout = 2000000000ull;
 
   if (threadIdx.x == 0) {
@@ -107,6 +111,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       bool ok = true;
       for (int pass = 0; pass < 2 && ok; ++pass) {
         for (int c = 0; c < nkv; ++c) {
+          if (!visible(c)) continue;
           const int st = it & 1;
           if (it >= 2 && !mbar_wait(&bars->kv_empty[st], ((it >> 1) - 1) & 1, wc, 1)) { ok = false; break; }
           mbar_arrive_expect_tx(&bars->kv_full[st], (pass == 0 ? 1 : 2) * C::kTileBytes);
@@ -135,6 +140,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       int it = 0, it2 = 0;
       for (int pass = 0; pass < 2 && ok; ++pass) {
         for (int c = 0; c < nkv; ++c) {
+          if (!visible(c)) continue;
           const int st = it & 1;
           const uint32_t sK = sbase + C::kOffK + st * C::kTileBytes;
           const uint32_t sV = sbase + C::kOffV + st * C::kTileBytes;
@@ -153,7 +159,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 #pragma unroll
             for (int k = 0; k < kTile / 16; ++k)
               mma_ts(tbase + C::kColO, tbase + C::kColP + 8 * k, desc_mnmajor(sV, k, 128), C::kIdO,
-                     !(c == 0 && k == 0));
+                     !(it2 == 0 && k == 0));
             mma_commit(&bars->o_done);
             mma_commit(&bars->kv_empty[st]);
             ++it2;
@@ -173,9 +179,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const bool causal = (p.mask == kMaskCausal);
     float m = -INFINITY, l = 0.f;
-    int it = 0;
+    int it = 0, nvis = 0;
     bool ok = true;
-    for (int c = 0; c < nkv && ok; ++c, ++it) {
+    for (int c = 0; c < nkv && ok; ++c) {
+      if (!visible(c)) continue;
+      ++nvis;
       if (!warp_wait(&bars->s_full, it & 1, wc, 30)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
@@ -201,9 +209,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_free);
+      ++it;
     }
-    const float lse2 = m + __log2f(l);
-    for (int c = 0, it2 = 0; c < nkv && ok; ++c, ++it, ++it2) {
+    const float lse2 = (nvis > 0) ? m + __log2f(l) : -INFINITY;
+    for (int c = 0, it2 = 0; c < nkv && ok; ++c) {
+      if (!visible(c)) continue;
       if (!warp_wait(&bars->s_full, it & 1, wc, 31)) { ok = false; break; }
       if (it2 > 0 && !warp_wait(&bars->o_done, (it2 - 1) & 1, wc, 32)) { ok = false; break; }
       tc_fence_after();
@@ -231,6 +241,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         mbar_arrive(&bars->s_free);
         mbar_arrive(&bars->p_full);
       }
+      ++it;
+      ++it2;
     }
     if (ok && warp_wait(&bars->o_full, 0, wc, 33)) {
       tc_fence_after();
@@ -239,6 +251,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       for (int ch = 0; ch < HD / 32; ++ch) {
         uint32_t v[32];
         tmem_ld32(tbase + lane_off + C::kColO + 32 * ch, v);
+        if (nvis == 0) {  // nothing visible: O = 0 (the accumulator was never written)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
         uint4* dst = reinterpret_cast<uint4*>(p.o + row * HD + 32 * ch);
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm)

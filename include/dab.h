@@ -131,6 +131,43 @@ dab_status_t dab_attn_bwd(const void* q, const void* k, const void* v,
                           void* workspace, size_t ws_bytes,
                           cudaStream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Block masks: the block-sparse masks the DASH pages name as future work
+ * (technical summary section 5).  `tiles` is a DEVICE array of N x N bytes,
+ * N = S/128, row j = query tile, column i = key tile, shared by all heads and
+ * caller-owned: a zero flag hides key tile i from every query of query tile
+ * j.  With causal = 1 the causal mask applies too (tiles above the diagonal
+ * are hidden whatever their flag, and the diagonal tiles hide keys after the
+ * query).  A query row with no visible key has no softmax: O = 0 and LSE =
+ * -infinity from the forward; its dQ is 0 and it adds nothing to dK, dV.
+ * A key tile no query sees gets dK = dV = 0.  Errors as dab_attn_fwd /
+ * dab_attn_bwd; tiles == NULL or causal not 0/1: DAB_ERR_INVALID_ARG.     */
+dab_status_t dab_attn_fwd_block(const void* q, const void* k, const void* v,
+                                void* o, float* lse,
+                                int B, int H, int S, int d, float scale,
+                                const uint8_t* tiles, int causal,
+                                void* workspace, size_t ws_bytes,
+                                cudaStream_t stream);
+
+/* Workspace of dab_attn_bwd_block: that of dab_attn_bwd plus the schedule
+ * tables built from the tile flags (0 for SHIFT, which is not available
+ * with a block mask, or on invalid arguments).                             */
+size_t dab_bwd_block_workspace_size(int B, int H, int S, int d, dab_sched_t sched);
+
+/* The backward under a block mask.  Schedules SERIAL, DESCENDING_Q (also for
+ * DAB_SCHED_AUTO) and ATOMIC: each KV tile walks its visible Q tiles only
+ * (ascending, or descending for DESCENDING_Q), and dQ_j adds its visible KV
+ * tiles' partial sums in ascending KV order, so SERIAL and DESCENDING_Q give
+ * the same dQ bits as without a mask.  SHIFT: DAB_ERR_UNSUPPORTED.  The
+ * preprocess kernel of the call builds the tables in the workspace.        */
+dab_status_t dab_attn_bwd_block(const void* q, const void* k, const void* v,
+                                const void* o, const float* lse, const void* dout,
+                                void* dq, void* dk, void* dv,
+                                int B, int H, int S, int d, float scale,
+                                const uint8_t* tiles, int causal, dab_sched_t sched,
+                                void* workspace, size_t ws_bytes,
+                                cudaStream_t stream);
+
 /* Synchronises `stream`, then reads the status word that the backward kernels
  * of the last call on this workspace wrote.  Returns DAB_OK, DAB_ERR_TIMEOUT
  * or DAB_ERR_DEVICE_BOUNDS (or DAB_ERR_CUDA if the synchronisation failed).  */

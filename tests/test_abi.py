@@ -109,6 +109,18 @@ def test_bad_arguments_rejected_without_touching_the_device(lib):
     assert hcall(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, p, 64, 0, None) == 3
     assert hcall(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, ctypes.c_void_p(16 + 256), big,
                  0, None) == 3
+    # block masks: null tile table, causal flag, SHIFT
+    assert lib.dab_attn_fwd_block(p, p, p, p, p, 1, 1, 256, 64, 0.125, nul, 0, nul, 0, None) == 1
+    assert lib.dab_attn_fwd_block(p, p, p, p, p, 1, 1, 256, 64, 0.125, p, 2, nul, 0, None) == 1
+    assert lib.dab_attn_bwd_block(p, p, p, p, p, p, p, p, p, 1, 1, 256, 64, 0.125, nul, 0, 0, p, big,
+                                  None) == 1
+    assert lib.dab_attn_bwd_block(p, p, p, p, p, p, p, p, p, 1, 1, 256, 64, 0.125, p, 0, 2, p, big,
+                                  None) == 2
+    assert lib.dab_bwd_block_workspace_size(1, 1, 256, 64, 2) == 0
+    assert lib.dab_bwd_block_workspace_size(1, 1, 256, 64, 1) > lib.dab_bwd_workspace_size(
+        1, 1, 256, 64, 0, 1)
+    assert lib.dab_bwd_block_workspace_size(1, 1, 256, 64, 4) == lib.dab_bwd_block_workspace_size(
+        1, 1, 256, 64, 1)
     # tensor-peak measurement: iteration count and status buffer are checked first
     assert lib.dab_mma_peak(0, p, None) == 1
     assert lib.dab_mma_peak(1 << 23, p, None) == 1
