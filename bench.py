@@ -39,8 +39,8 @@ DET_SCHEDS = ("serial", "descending_q", "shift")
 # number of heads, so x2), keyed by the SHA-1 of the kernel source it was
 # taken on.  Reported only while the source is unchanged.
 TRAFFIC_CAPTURES = {
-    # causal 136.7 + 276.4 MB, full 138.6 + 294.0 MB: mean of the masks, x2
-    "47b61baf0fa4537fe9081a3c62c2a0eca14d8a61": 2 * ((136.651520 + 276.430592) + (138.601216 + 293.974528)) / 2 * 1e6,
+    # causal 136.5 + 275.9 MB, full 137.8 + 294.9 MB: mean of the masks, x2
+    "79d614cbbad8a1299646493577fe493f47aef035": 2 * ((136.491776 + 275.88864) + (137.788928 + 294.857216)) / 2 * 1e6,
 }
 MASKS = ("causal", "full")
 
