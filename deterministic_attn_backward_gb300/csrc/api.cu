@@ -18,7 +18,7 @@
 namespace dab {
 // kernels (bwd.cu, fwd.cu, aux.cu, selftest.cu)
 template <int HD> int bwd_smem_bytes();
-template <int HD> const void* bwd_kernel_ptr();
+template <int HD> const void* bwd_kernel_ptr(bool ragged);
 template <int HD> int fwd_smem_bytes();
 template <int HD> const void* fwd_kernel_ptr();
 template <int HD> int selftest_smem_bytes();
@@ -28,7 +28,7 @@ const void* peak_kernel_ptr();
 int peak_threads();
 cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const float* lse, float* D,
                               float* lse2, uint32_t* sem, int n_sem, WsHeader* hdr, float* dqacc,
-                              long long dq_elems, int rows, int grid, cudaStream_t stream);
+                              long long dq_elems, int BH, int S, int S_pad, int grid, cudaStream_t stream);
 cudaError_t launch_convert(const float* dqacc, void* dq, long long elems, float scale,
                            long long acc_stride, int ways, int causal, int N, int S, int d, int grid,
                            const int* count, cudaStream_t stream);
@@ -73,10 +73,12 @@ bool device_setup(int* dev_out, int* sms_out) {
     di.supported = (prop.major == 10 && prop.minor == 3);
     if (di.supported) {
       bool ok = true;
-      ok &= cudaFuncSetAttribute(dab::bwd_kernel_ptr<64>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 dab::bwd_smem_bytes<64>()) == cudaSuccess;
-      ok &= cudaFuncSetAttribute(dab::bwd_kernel_ptr<128>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 dab::bwd_smem_bytes<128>()) == cudaSuccess;
+      for (bool ragged : {false, true}) {
+        ok &= cudaFuncSetAttribute(dab::bwd_kernel_ptr<64>(ragged), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   dab::bwd_smem_bytes<64>()) == cudaSuccess;
+        ok &= cudaFuncSetAttribute(dab::bwd_kernel_ptr<128>(ragged), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   dab::bwd_smem_bytes<128>()) == cudaSuccess;
+      }
       ok &= cudaFuncSetAttribute(dab::fwd_kernel_ptr<64>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  dab::fwd_smem_bytes<64>()) == cudaSuccess;
       ok &= cudaFuncSetAttribute(dab::fwd_kernel_ptr<128>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -130,12 +132,18 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Any sequence length: the last 128-row tile of a head may be partial.  B, H
+// or S of zero is an empty problem (nothing to compute, DAB_OK).
 dab_status_t check_shape(int B, int H, int S, int d) {
-  if (B < 1 || H < 1 || S < 128 || (S % 128) != 0) return DAB_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || S < 0) return DAB_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return DAB_ERR_INVALID_ARG;
-  if ((long long)B * H * S >= (1ll << 31)) return DAB_ERR_INVALID_ARG;
+  if ((long long)B * H * (((long long)S + 127) / 128 * 128) >= (1ll << 31)) return DAB_ERR_INVALID_ARG;
   return DAB_OK;
 }
+
+bool empty_problem(int B, int H, int S) { return (long long)B * H * S == 0; }
+
+int tiles_of(int S) { return (S + 127) / 128; }
 
 dab_status_t check_enums(dab_mask_t mask, dab_sched_t sched) {
   if ((int)mask < 0 || (int)mask > 1) return DAB_ERR_INVALID_ARG;
@@ -167,7 +175,8 @@ int acc_ways(dab_sched_t sched) { return sched == DAB_SCHED_ATOMIC ? 1 : dab::kA
 
 bool layout(int B, int H, int S, int d, dab_sched_t sched, dab_ws_layout_t* L) {
   if (check_shape(B, H, S, d) != DAB_OK) return false;
-  const size_t BH = (size_t)B * H, N = (size_t)S / 128, rows = BH * S;
+  const size_t BH = (size_t)B * H, N = (size_t)tiles_of(S), rows = BH * S;
+  const size_t rows_pad = BH * N * 128;  // D and LSE2 per head padded to whole tiles
   const size_t ways = (size_t)acc_ways(sched);
   size_t off = 0;
   L->status = off;
@@ -175,9 +184,9 @@ bool layout(int B, int H, int S, int d, dab_sched_t sched, dab_ws_layout_t* L) {
   L->sem = off;
   off = round_up(off + BH * N * dab::kSubTiles * ways * 4, 256);  // per tile, sub-tile, buffer
   L->D = off;
-  off = round_up(off + rows * 4, 256);
+  off = round_up(off + rows_pad * 4, 256);
   L->lse2 = off;
-  off = round_up(off + rows * 4, 256);
+  off = round_up(off + rows_pad * 4, 256);
   L->dqacc = off;
   off = round_up(off + ways * rows * (size_t)d * 4, 256);
   L->total = off;
@@ -243,6 +252,7 @@ static dab_status_t fwd_impl(const void* q, const void* k, const void* v, void* 
                              int H, int S, int d, float scale, dab_mask_t mask, void* workspace,
                              size_t ws_bytes, cudaStream_t stream, const uint8_t* tiles) {
   if (check_shape(B, H, S, d) != DAB_OK) return DAB_ERR_INVALID_ARG;
+  if (empty_problem(B, H, S)) return DAB_OK;
   if ((int)mask < 0 || (int)mask > 1) return DAB_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return DAB_ERR_INVALID_ARG;
@@ -259,7 +269,7 @@ static dab_status_t fwd_impl(const void* q, const void* k, const void* v, void* 
   p.lse = lse;
   p.BH = B * H;
   p.S = S;
-  p.N = S / 128;
+  p.N = tiles_of(S);
   p.mask = (int)mask;
   p.scale_log2e = scale * 1.4426950408889634f;
   p.tiles = tiles;
@@ -284,7 +294,7 @@ dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v, void* o, 
 dab_status_t dab_attn_fwd_block(const void* q, const void* k, const void* v, void* o, float* lse,
                                 int B, int H, int S, int d, float scale, const uint8_t* tiles,
                                 int causal, void* workspace, size_t ws_bytes, cudaStream_t stream) {
-  if (tiles == nullptr || (causal != 0 && causal != 1)) return DAB_ERR_INVALID_ARG;
+  if (tiles == nullptr || (causal != 0 && causal != 1) || (S % 128) != 0) return DAB_ERR_INVALID_ARG;
   return fwd_impl(q, k, v, o, lse, B, H, S, d, scale, causal ? DAB_MASK_CAUSAL : DAB_MASK_FULL,
                   workspace, ws_bytes, stream, tiles);
 }
@@ -293,6 +303,7 @@ dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dou
                                 int d, dab_mask_t mask, dab_sched_t sched, void* workspace,
                                 size_t ws_bytes, cudaStream_t stream) {
   if (check_shape(B, H, S, d) != DAB_OK || check_enums_auto(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
+  if (empty_problem(B, H, S)) return DAB_OK;
   if (!aligned16(o) || !aligned16(lse) || !aligned16(dout)) return DAB_ERR_INVALID_ARG;
   if (sched == DAB_SCHED_AUTO) sched = DAB_SCHED_DESCENDING_Q;  // same preprocessing for all ordered schedules
   dab_ws_layout_t L;
@@ -303,13 +314,13 @@ dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dou
   if (!device_setup(nullptr, &sms)) return DAB_ERR_UNSUPPORTED;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const long long rows = (long long)B * H * S;
-  const int n_sem = B * H * (S / 128) * dab::kSubTiles * acc_ways(sched);
+  const int n_sem = B * H * tiles_of(S) * dab::kSubTiles * acc_ways(sched);
   float* dqacc = (sched == DAB_SCHED_ATOMIC) ? reinterpret_cast<float*>(ws + L.dqacc) : nullptr;
   const int grid = elementwise_grid(sms, rows * (d / 8));
   cudaError_t e = dab::launch_preprocess(
       d, o, dout, lse, reinterpret_cast<float*>(ws + L.D), reinterpret_cast<float*>(ws + L.lse2),
       reinterpret_cast<uint32_t*>(ws + L.sem), n_sem, reinterpret_cast<dab::WsHeader*>(ws + L.status),
-      dqacc, rows * d, (int)rows, grid, stream);
+      dqacc, rows * d, B * H, S, tiles_of(S) * 128, grid, stream);
   return e == cudaSuccess ? DAB_OK : cuda_fail(e, "preprocess launch");
 }
 
@@ -320,11 +331,13 @@ static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const 
                              void* workspace, size_t ws_bytes, cudaStream_t stream,
                              const dab_bwd_opts_t* opts, const uint8_t* tiles) {
   if (check_shape(B, H, S, d) != DAB_OK || check_enums_auto(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
+  if (empty_problem(B, H, S)) return DAB_OK;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return DAB_ERR_INVALID_ARG;
   if (!(scale > 0.f)) return DAB_ERR_INVALID_ARG;
   const bool block = tiles != nullptr;
+  if (block && (S % 128) != 0) return DAB_ERR_INVALID_ARG;  // block masks cover whole tiles
   if (block) {
     if (sched == DAB_SCHED_AUTO) sched = DAB_SCHED_DESCENDING_Q;
     if (sched == DAB_SCHED_SHIFT) return DAB_ERR_UNSUPPORTED;  // no shift walk over a block mask
@@ -332,7 +345,7 @@ static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const 
     const dab_status_t st = resolve_sched(mask, B, H, S, (opts && opts->grid > 0) ? opts->grid : 0, &sched);
     if (st != DAB_OK) return st;
   }
-  const int N = S / 128;
+  const int N = tiles_of(S);
   if (sched == DAB_SCHED_SHIFT && mask == DAB_MASK_CAUSAL && (N % 2) != 0) return DAB_ERR_UNSUPPORTED;
   dab_ws_layout_t L;
   layout(B, H, S, d, sched, &L);
@@ -415,7 +428,9 @@ static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const 
   void* args[] = {&p};
   cudaError_t e = cudaSuccess;
   if (!(flags & DAB_BWD_SKIP_MAIN)) {
-    e = cudaLaunchKernelExC(&cfg, d == 128 ? dab::bwd_kernel_ptr<128>() : dab::bwd_kernel_ptr<64>(), args);
+    const bool ragged = (S % 128) != 0;
+    e = cudaLaunchKernelExC(&cfg, d == 128 ? dab::bwd_kernel_ptr<128>(ragged) : dab::bwd_kernel_ptr<64>(ragged),
+                            args);
     if (e != cudaSuccess) return cuda_fail(e, "main kernel launch");
   }
 
@@ -443,7 +458,7 @@ size_t dab_bwd_block_workspace_size(int B, int H, int S, int d, dab_sched_t sche
   if (sched == DAB_SCHED_AUTO) sched = DAB_SCHED_DESCENDING_Q;
   dab_ws_layout_t L;
   if (check_enums(DAB_MASK_FULL, sched) != DAB_OK || !layout(B, H, S, d, sched, &L)) return 0;
-  return block_tables_layout(L, S / 128).total;
+  return block_tables_layout(L, tiles_of(S)).total;
 }
 
 dab_status_t dab_attn_bwd_block(const void* q, const void* k, const void* v, const void* o,

@@ -35,12 +35,16 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b) {
 }
 
 // One row of HD bf16 is HD/8 vectors; a warp covers 32 / (HD/8) rows at once.
+// D and LSE2 are laid out per head with S_pad = 128 * ceil(S / 128) rows; the
+// rows past S of a partial last tile get D = 0 and LSE2 = +infinity, so that
+// every P the main kernel forms for them is exactly 0.
 template <int HD>
 __global__ void __launch_bounds__(256) preprocess_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
     const float* __restrict__ lse, float* __restrict__ D, float* __restrict__ lse2,
     uint32_t* __restrict__ sem, int n_sem, WsHeader* __restrict__ hdr,
-    float4* __restrict__ dqacc, long long dq_vec4, int rows) {
+    float4* __restrict__ dqacc, long long dq_vec4, int BH, int S, int S_pad) {
+  const int rows = BH * S;
   constexpr int kLanesPerRow = HD / 8;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const int lane = threadIdx.x & 31;
@@ -55,6 +59,14 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
     hdr->ticket = 0u;
   }
   for (long long i = gtid; i < n_sem; i += nthreads) sem[i] = 0u;
+  if (S_pad > S) {
+    const long long npad = (long long)BH * (S_pad - S);
+    for (long long i = gtid; i < npad; i += nthreads) {
+      const long long idx = (i / (S_pad - S)) * S_pad + S + i % (S_pad - S);
+      D[idx] = 0.f;
+      lse2[idx] = INFINITY;
+    }
+  }
   if (dqacc != nullptr) {
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     for (long long i = gtid; i < dq_vec4; i += nthreads) dqacc[i] = z;
@@ -74,8 +86,11 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
     for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
       acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (row < rows && part == 0) {
-      D[row] = acc;
-      lse2[row] = lse[row] * kLog2e;
+      // padded per-head index (rows < 2^31: 32-bit arithmetic)
+      const int ir = (int)row;
+      const int idx = (S_pad == S) ? ir : (ir / S) * S_pad + ir % S;
+      D[idx] = acc;
+      lse2[idx] = lse[row] * kLog2e;
     }
   }
 }
@@ -159,17 +174,18 @@ cudaError_t launch_block_tables(const uint8_t* tiles, int N, int causal, int des
 
 cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const float* lse, float* D,
                               float* lse2, uint32_t* sem, int n_sem, WsHeader* hdr, float* dqacc,
-                              long long dq_elems, int rows, int grid, cudaStream_t stream) {
+                              long long dq_elems, int BH, int S, int S_pad, int grid,
+                              cudaStream_t stream) {
   float4* z = reinterpret_cast<float4*>(dqacc);
   const long long nv = dqacc ? dq_elems / 4 : 0;
   if (HD == 128) {
     preprocess_kernel<128><<<grid, 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, D, lse2,
-        sem, n_sem, hdr, z, nv, rows);
+        sem, n_sem, hdr, z, nv, BH, S, S_pad);
   } else {
     preprocess_kernel<64><<<grid, 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, D, lse2,
-        sem, n_sem, hdr, z, nv, rows);
+        sem, n_sem, hdr, z, nv, BH, S, S_pad);
   }
   return cudaGetLastError();
 }

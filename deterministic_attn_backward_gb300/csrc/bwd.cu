@@ -132,7 +132,10 @@ __device__ __forceinline__ int k_rank(const BwdParams& p, int i, int j) {
   return p.sched == kSchedAtomic ? -1 : (int)p.blk_rank[(size_t)j * p.N + i];
 }
 
-template <int HD>
+// kRagged: S is not a multiple of the tile, so the last tile of each head is
+// partial (masked keys, rows never written).  A separate instance, so that the
+// common case carries none of those checks.
+template <int HD, bool kRagged>
 __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = Cfg<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -236,8 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             tma_load_2d(sq + db * C::kBlockBytes, &p.tm_q, &bars->q_full[stage], db * 64, row);
             tma_load_2d(sdo + db * C::kBlockBytes, &p.tm_do, &bars->q_full[stage], db * 64, row);
           }
-          bulk_load(s_lse + stage * 128, p.lse2 + row, 512, &bars->q_full[stage]);
-          bulk_load(s_dd + stage * 128, p.D + row, 512, &bars->q_full[stage]);
+          // LSE2 and D are padded to whole tiles per head (+inf / 0 past S)
+          const size_t prow = (size_t)bh * (p.N * kTile) + (size_t)st.q * kTile;
+          bulk_load(s_lse + stage * 128, p.lse2 + prow, 512, &bars->q_full[stage]);
+          bulk_load(s_dd + stage * 128, p.D + prow, 512, &bars->q_full[stage]);
           ++issued[stage];
           ++s;
         }
@@ -394,10 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       const int steps = k_unit_steps(p, u);
       if (steps == 0) {
         // A KV tile that no visible Q tile meets (block mask): dK = dV = 0.
-        const size_t row = (size_t)bh * p.S + (size_t)u * kTile + r;
-        uint4* dst = reinterpret_cast<uint4*>((h == 0 ? p.dv : p.dk) + row * HD);
+        if (!kRagged || u * kTile + r < p.S) {
+          const size_t row = (size_t)bh * p.S + (size_t)u * kTile + r;
+          uint4* dst = reinterpret_cast<uint4*>((h == 0 ? p.dv : p.dk) + row * HD);
 #pragma unroll
-        for (int c = 0; c < HD / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+          for (int c = 0; c < HD / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
         continue;
       }
       for (int t = 0; t < steps; ++t) {
@@ -406,6 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         const float* lse = s_lse + stage * 128 + 64 * h;
         const float* dd = s_dd + stage * 128 + 64 * h;
         const bool diag = (p.mask == kMaskCausal) && (st.kv == st.q);
+        // a key past the end of a partial last tile: its whole P row is 0
+        // (applied to the packed words below; `key_out` only on such a tile)
+        const bool key_out = (st.kv * kTile + r) >= p.S;
+        const bool tail_kv = kRagged && (st.kv + 1) * kTile > p.S;  // uniform: a partial last KV tile
         if (!warp_wait(&bars->q_full[stage], (s >> 1) & 1, wc, 31)) { ok = false; break; }
         if (!warp_wait(&bars->s_full, s & 1, wc, 32)) { ok = false; break; }
         tc_fence_after();
@@ -436,6 +447,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             w16[(e >> 1) + 1] = pack_bf16x2(p2, p3);
             pk[16 * c + (e >> 1)] = w16[e >> 1];
             pk[16 * c + (e >> 1) + 1] = w16[(e >> 1) + 1];
+          }
+          if (tail_kv && key_out) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              w16[x] = 0u;
+              pk[16 * c + x] = 0u;
+            }
           }
           tmem_st16(tbase + lane_off + C::kColS + 64 * h + 16 * c, w16);
         }
@@ -484,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           if (!warp_wait(&bars->acc_full, chain & 1, wc, 35)) { ok = false; break; }
           tc_fence_after();
           const size_t row = (size_t)bh * p.S + (size_t)st.kv * kTile + r;
+          const bool row_in = !kRagged || st.kv * kTile + r < p.S;  // rows of a partial last tile
           __nv_bfloat16* out = (h == 0 ? p.dv : p.dk) + row * HD;
           const uint32_t col0 = (h == 0) ? C::kColDV : C::kColDK;
           const float sc = (h == 0) ? 1.0f : p.scale;
@@ -494,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             uint4* dst = reinterpret_cast<uint4*>(out + 16 * c);
 #pragma unroll
             for (int m = 0; m < 2; ++m)
-              dst[m] = make_uint4(
+              if (row_in) dst[m] = make_uint4(
                   pack_bf16x2(sc * __uint_as_float(v[8 * m]), sc * __uint_as_float(v[8 * m + 1])),
                   pack_bf16x2(sc * __uint_as_float(v[8 * m + 2]), sc * __uint_as_float(v[8 * m + 3])),
                   pack_bf16x2(sc * __uint_as_float(v[8 * m + 4]), sc * __uint_as_float(v[8 * m + 5])),
@@ -559,6 +578,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         float* acc = p.dqacc + (size_t)way * (size_t)p.acc_stride;
         float* base = (HD == 128) ? acc + (row0 + (size_t)half * 64) * HD + r
                                   : acc + (row0 + (size_t)r) * HD + half * 32;
+        // Rows past the end of a partial last Q tile belong to the next head
+        // in the accumulator: never touched (their partial sums are zero).
+        const int row_lim = p.S - st.q * kTile - ((HD == 128) ? half * 64 : r);
+        const int nvalid = !kRagged ? ((HD == 128) ? 64 : 1)
+                           : (HD == 128) ? (row_lim < 0 ? 0 : (row_lim > 64 ? 64 : row_lim))
+                                         : (row_lim > 0 ? 1 : 0);
         if (!warp_wait(&bars->dq_full, s & 1, wc, 41)) { ok = false; break; }
         tc_fence_after();
         uint32_t v[kVals];
@@ -583,8 +608,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         }
         if (HD == 128) {
           if (store) {
+            if (nvalid == 64) {
 #pragma unroll
-            for (int q = 0; q < 64; ++q) base[(size_t)q * HD] = __uint_as_float(v[q]);
+              for (int q = 0; q < 64; ++q) base[(size_t)q * HD] = __uint_as_float(v[q]);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 64; ++q)
+                if (q < nvalid) base[(size_t)q * HD] = __uint_as_float(v[q]);
+            }
           } else if (deterministic && p.plain_add) {
             // load + add + store, the same IEEE adds in the same order as
             // the red (only this contributor touches the sub-tile now)
@@ -593,23 +624,32 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             for (int c = 0; c < 64; c += 16) {
               float a[16];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) a[k] = ld_cg_f32(base + (size_t)(c + k) * HD);
+              for (int k = 0; k < 16; ++k)
+                a[k] = (c + k < nvalid) ? ld_cg_f32(base + (size_t)(c + k) * HD) : 0.f;
 #pragma unroll
-              for (int k = 0; k < 16; ++k) base[(size_t)(c + k) * HD] = a[k] + __uint_as_float(v[c + k]);
+              for (int k = 0; k < 16; ++k)
+                if (c + k < nvalid) base[(size_t)(c + k) * HD] = a[k] + __uint_as_float(v[c + k]);
             }
           } else {
+            if (nvalid == 64) {
 #pragma unroll
-            for (int q = 0; q < 64; ++q) {
-              red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
-              // Ordered schedules: spread the adds out so that they do not
-              // fill the SM's memory-instruction queue in one burst (the
-              // softmax warps' shared-memory loads wait behind them).
-              if (deterministic && (q & 7) == 7) __nanosleep(20);
+              for (int q = 0; q < 64; ++q) {
+                red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
+                // Ordered schedules: spread the adds out so that they do not
+                // fill the SM's memory-instruction queue in one burst (the
+                // softmax warps' shared-memory loads wait behind them).
+                if (deterministic && (q & 7) == 7) __nanosleep(20);
+              }
+            } else {  // the last, partial Q tile
+#pragma unroll
+              for (int q = 0; q < 64; ++q)
+                if (q < nvalid) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
             }
           }
         } else {
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
+            if (nvalid == 0) break;                  // this Q row lies past S
             const float a0 = __uint_as_float(v[4 * m]), a1 = __uint_as_float(v[4 * m + 1]);
             const float a2 = __uint_as_float(v[4 * m + 2]), a3 = __uint_as_float(v[4 * m + 3]);
             if (store) {
@@ -657,13 +697,14 @@ int bwd_smem_bytes() {
 }
 
 template <int HD>
-const void* bwd_kernel_ptr() {
-  return reinterpret_cast<const void*>(&bwd_kernel<HD>);
+const void* bwd_kernel_ptr(bool ragged) {
+  return ragged ? reinterpret_cast<const void*>(&bwd_kernel<HD, true>)
+                : reinterpret_cast<const void*>(&bwd_kernel<HD, false>);
 }
 
 template int bwd_smem_bytes<64>();
 template int bwd_smem_bytes<128>();
-template const void* bwd_kernel_ptr<64>();
-template const void* bwd_kernel_ptr<128>();
+template const void* bwd_kernel_ptr<64>(bool);
+template const void* bwd_kernel_ptr<128>(bool);
 
 }  // namespace dab

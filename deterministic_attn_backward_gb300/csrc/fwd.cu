@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const int col = 32 * ch + e;
           x[e] = __uint_as_float(v[e]) * p.scale_log2e;
           if (causal && c == qi && col > r) x[e] = -INFINITY;
+          if (c * kTile + col >= p.S) x[e] = -INFINITY;   // past the end of a partial last tile
           cmax = fmaxf(cmax, x[e]);
         }
         const float mn = fmaxf(m, cmax);
@@ -231,6 +232,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             if (col > r) p0 = 0.f;
             if (col + 1 > r) p1 = 0.f;
           }
+          if (c * kTile + col >= p.S) p0 = 0.f;
+          if (c * kTile + col + 1 >= p.S) p1 = 0.f;
           w16[e >> 1] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tbase + lane_off + C::kColP + 16 * ch, w16);
@@ -247,6 +250,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     if (ok && warp_wait(&bars->o_full, 0, wc, 33)) {
       tc_fence_after();
       const size_t row = (size_t)bh * p.S + (size_t)qi * kTile + r;
+      const bool row_in = qi * kTile + r < p.S;  // rows of a partial last tile
 #pragma unroll
       for (int ch = 0; ch < HD / 32; ++ch) {
         uint32_t v[32];
@@ -258,12 +262,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         uint4* dst = reinterpret_cast<uint4*>(p.o + row * HD + 32 * ch);
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm)
-          dst[mm] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * mm]), __uint_as_float(v[8 * mm + 1])),
+          if (row_in) dst[mm] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * mm]), __uint_as_float(v[8 * mm + 1])),
                                pack_bf16x2(__uint_as_float(v[8 * mm + 2]), __uint_as_float(v[8 * mm + 3])),
                                pack_bf16x2(__uint_as_float(v[8 * mm + 4]), __uint_as_float(v[8 * mm + 5])),
                                pack_bf16x2(__uint_as_float(v[8 * mm + 6]), __uint_as_float(v[8 * mm + 7])));
       }
-      p.lse[row] = lse2 * kLn2;
+      if (row_in) p.lse[row] = lse2 * kLn2;
     }
   }
   tc_fence_before();

@@ -87,6 +87,8 @@ bool host_layout(int B, int H, int S, int d, dab_mask_t mask, dab_sched_t sched,
 
 extern "C" size_t dab_bwd_host_workspace_size(int B, int H, int S, int d, dab_mask_t mask,
                                               dab_sched_t sched, int chunks) {
+  if (B >= 0 && H >= 0 && S >= 0 && (long long)B * H * S == 0)  // empty problem
+    return dab_bwd_workspace_size(B, H, S, d, mask, sched) ? 256 : 0;
   HostLayout L;
   return host_layout(B, H, S, d, mask, sched, chunks, &L) ? L.total : 0;
 }
@@ -97,6 +99,8 @@ extern "C" dab_status_t dab_attn_bwd_host(const void* q, const void* k, const vo
                                           float scale, dab_mask_t mask, dab_sched_t sched,
                                           void* dev_ws, size_t dev_ws_bytes, int chunks,
                                           cudaStream_t stream) {
+  if (B >= 0 && H >= 0 && S >= 0 && (long long)B * H * S == 0)  // empty problem: nothing to do
+    return dab_bwd_workspace_size(B, H, S, d, mask, sched) ? DAB_OK : DAB_ERR_INVALID_ARG;
   HostLayout L;
   if (!host_layout(B, H, S, d, mask, sched, chunks, &L)) return DAB_ERR_INVALID_ARG;
   for (const void* p : {q, k, v, o, static_cast<const void*>(lse), dout,

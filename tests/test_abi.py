@@ -65,7 +65,12 @@ def test_workspace_layout(lib):
     for off in (L.sem, L.D, L.lse2, L.dqacc, L.total):
         assert off % 256 == 0
     assert dab.workspace_size(B, H, S, d, "causal", "descending_q") == L.total
-    assert lib.dab_bwd_workspace_size(B, H, 100, d, 0, 0) == 0      # S not a multiple of 128
+    # any S: a partial last tile pads D and LSE2 to whole tiles per head
+    Lr = dab.workspace_layout(B, H, 200, d, "full", "serial")
+    assert Lr.lse2 >= Lr.D + 4 * B * H * 256 and Lr.dqacc >= Lr.lse2 + 4 * B * H * 256
+    assert Lr.total >= Lr.dqacc + 4 * 4 * B * H * 200 * d
+    assert lib.dab_bwd_workspace_size(B, H, 0, d, 0, 0) > 0            # empty problem
+    assert lib.dab_bwd_workspace_size(B, H, -1, d, 0, 0) == 0          # negative length
     assert lib.dab_bwd_workspace_size(B, H, S, 96, 0, 0) == 0       # d not 64/128
     assert lib.dab_bwd_workspace_size(B, H, S, d, 2, 0) == 0        # bad mask
 
@@ -80,7 +85,7 @@ def test_bad_arguments_rejected_without_touching_the_device(lib):
     assert call(ctypes.c_void_p(17), p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, p, big,
                 None) == 1
     # bad shape / enum / scale
-    assert call(p, p, p, p, p, p, p, p, p, 1, 1, 192, 64, 0.125, 0, 0, p, big, None) == 1
+    assert call(p, p, p, p, p, p, p, p, p, 1, 1, -128, 64, 0.125, 0, 0, p, big, None) == 1
     assert call(p, p, p, p, p, p, p, p, p, 1, 1, 128, 80, 0.125, 0, 0, p, big, None) == 1
     assert call(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 7, p, big, None) == 1
     assert call(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, -1.0, 0, 0, p, big, None) == 1
@@ -96,12 +101,12 @@ def test_bad_arguments_rejected_without_touching_the_device(lib):
     # DAB_SCHED_AUTO (4): accepted by the backward entry points, not by the
     # schedule introspection functions
     assert lib.dab_sched_units_per_head(4, 0, 8) == -1
-    assert call(p, p, p, p, p, p, p, p, p, 1, 1, 192, 64, 0.125, 0, 4, p, big, None) == 1
+    assert call(p, p, p, p, p, p, p, p, p, 1, 1, -128, 64, 0.125, 0, 4, p, big, None) == 1
     assert call(p, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 5, p, big, None) == 1
     # host-buffer path: sizes, null pointers and workspace checked before any CUDA call
     assert lib.dab_bwd_host_workspace_size(2, 3, 640, 128, 0, 0, 2) > lib.dab_bwd_workspace_size(
         1, 3, 640, 128, 0, 0)
-    assert lib.dab_bwd_host_workspace_size(2, 3, 600, 128, 0, 0, 2) == 0
+    assert lib.dab_bwd_host_workspace_size(2, 3, -600, 128, 0, 0, 2) == 0
     assert lib.dab_bwd_host_workspace_size(2, 3, 640, 80, 0, 0, 2) == 0
     hcall = lambda *a: lib.dab_attn_bwd_host(*a)
     assert hcall(nul, p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0.125, 0, 0, p, big, 0, None) == 1
