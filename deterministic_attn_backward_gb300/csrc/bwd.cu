@@ -455,8 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
               pk[16 * c + x] = 0u;
             }
           }
-          tmem_st16(tbase + lane_off + C::kColS + 64 * h + 16 * c, w16);
+          tmem_st16_nowait(tbase + lane_off + C::kColS + 64 * h + 16 * c, w16);
         }
+        tmem_st_wait_all();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full);
