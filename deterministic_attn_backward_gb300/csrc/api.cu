@@ -406,6 +406,12 @@ static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const 
   p.scale_log2e = scale * 1.4426950408889634f;
   p.timeout_ns = timeout;
   p.plain_add = (flags & DAB_BWD_PLAIN_ADD) ? 1 : 0;
+  // The ordered schedules finalise dQ in the main kernel's tail unless the
+  // caller asks for the separate pass (or skips the main kernel or the convert).
+  p.fuse_convert = (sched != DAB_SCHED_ATOMIC &&
+                    !(flags & (DAB_BWD_SEPARATE_CONVERT | DAB_BWD_SKIP_CONVERT | DAB_BWD_SKIP_MAIN)))
+                       ? 1 : 0;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
   if (block) {
     p.block = 1;
     p.blk_list = reinterpret_cast<const uint16_t*>(ws + T.list);
@@ -434,7 +440,7 @@ static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const 
     if (e != cudaSuccess) return cuda_fail(e, "main kernel launch");
   }
 
-  if (!(flags & DAB_BWD_SKIP_CONVERT)) {
+  if (!(flags & DAB_BWD_SKIP_CONVERT) && !p.fuse_convert) {
     const long long elems = rows * d;
     e = dab::launch_convert(p.dqacc, dq, elems, scale, p.acc_stride, p.acc_ways,
                             mask == DAB_MASK_CAUSAL ? 1 : 0, N, S, d, elementwise_grid(sms, elems / 4),

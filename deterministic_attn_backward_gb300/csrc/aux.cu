@@ -3,10 +3,12 @@
 // preprocess: D_r = sum_k dO_rk O_rk in f32 (the row term of
 //             dS = P o (dP - D)), LSE_r * log2(e) for the base-2 softmax
 //             recomputation, and the reset of everything the main kernel
-//             needs at zero (status word, dispatch counter, dQ semaphores;
+//             needs at zero (status word, dispatch counters, dQ semaphores;
 //             the f32 dQ accumulator too for the unordered atomic schedule).
 // convert:    dQ = bf16(scale * (dQacc_0 + dQacc_1 + ...)), the accumulation
-//             buffers added in index order.
+//             buffers added in index order.  The ordered schedules do the same
+//             arithmetic inside the main kernel by default; this pass serves
+//             the atomic schedule and callers that ask for a separate pass.
 // Both are grid-stride loops over 16-byte vectors, sized to a multiple of the
 // SM count by the host.
 #include <cuda_bf16.h>
@@ -57,6 +59,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
     hdr->status = 0u;
     hdr->detail = 0u;
     hdr->ticket = 0u;
+    hdr->conv_ticket = 0u;
   }
   for (long long i = gtid; i < n_sem; i += nthreads) sem[i] = 0u;
   if (S_pad > S) {

@@ -86,6 +86,7 @@ struct Misc {
   uint32_t tmem_base;
   int abort;
   int ring[2];
+  int conv;  // dQ tile being finalised in the tail, or -1
 };
 static_assert(sizeof(Misc) <= 64, "misc block");
 
@@ -130,6 +131,101 @@ __device__ __forceinline__ Step k_step(const BwdParams& p, int u, int t, int ste
 __device__ __forceinline__ int k_rank(const BwdParams& p, int i, int j) {
   if (!p.block) return rank(p.sched, p.mask, p.N, i, j);
   return p.sched == kSchedAtomic ? -1 : (int)p.blk_rank[(size_t)j * p.N + i];
+}
+
+// Bounded wait for a dQ semaphore to reach its final value, polled gently:
+// the waiting CTA has no other work, and the CTAs still running share the L2.
+static __device__ __noinline__ bool final_wait(const uint32_t* sem, uint32_t target,
+                                               const WaitCtl& w, uint32_t detail) {
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(sem) != target) {
+    if (*w.abort) return false;
+    if (ld_volatile(&w.hdr->status) != 0u) {
+      *w.abort = 1;
+      return false;
+    }
+    if (globaltimer_ns() - t0 > w.timeout_ns) {
+      raise_error(w.hdr, kStatusTimeout, kDetailSem | (detail & 0xFFFFFFu));
+      *w.abort = 1;
+      return false;
+    }
+    __nanosleep(200);
+  }
+  return true;
+}
+
+// dQ finalisation in the kernel's tail (ordered schedules).  A CTA that has
+// run out of units claims whole dQ tiles (bh, j) from a second counter, in
+// head order and, within a head, in the order the schedule completes them.
+// A tile is final once every (sub-tile, buffer) semaphore holds the number of
+// contributions that buffer receives: for c contributors and W buffers,
+// buffer m < min(c, W) receives (c - 1 - m) / W + 1 of them.  Every unit has
+// been claimed by a running CTA before any tile is, and no unit waits for a
+// tile, so these waits always end.  The arithmetic is the convert pass's:
+// the buffers added in index order, times scale, rounded to bf16 (RN-even),
+// so dQ has the same bits whichever of the two wrote it.
+template <int HD, bool kRagged>
+__device__ __forceinline__ void tail_convert(const BwdParams& p, Misc* misc, const WaitCtl& wc) {
+  const int tid = threadIdx.x;
+  const int ntiles = p.BH * p.N;
+  const size_t stride4 = (size_t)p.acc_stride / 4;
+  while (true) {
+    if (tid == 0) {
+      const int T = misc->abort ? ntiles : (int)atomicAdd(&p.hdr->conv_ticket, 1u);
+      misc->conv = (T < ntiles) ? T : -1;
+    }
+    __syncthreads();
+    const int T = misc->conv;
+    if (T < 0) break;
+    const int bh = T / p.N, jj = T % p.N;
+    const int j = (p.sched == kSchedDescending) ? p.N - 1 - jj : jj;
+    const int c = p.block ? p.blk_count[j] : (p.mask == kMaskCausal ? j + 1 : p.N);
+    const int nacc = c < p.acc_ways ? c : p.acc_ways;
+    int ok = 1;
+    if (tid < kSubTiles * nacc) {
+      const int sub = tid / nacc, way = tid % nacc;
+      const size_t sem_idx = (((size_t)bh * p.N + j) * kSubTiles + sub) * p.acc_ways + way;
+      const uint32_t target = (uint32_t)((c - 1 - way) / p.acc_ways + 1);
+      ok = final_wait(p.sem + sem_idx, target, wc, (uint32_t)sem_idx) ? 1 : 0;
+    }
+    if (!__syncthreads_and(ok)) break;
+    fence_acq_rel_gpu();
+    // rows of the tile inside the head (a partial last tile stops at S)
+    const int rows = kRagged ? min(kTile, p.S - j * kTile) : kTile;
+    const size_t e0 = ((size_t)bh * p.S + (size_t)j * kTile) * HD;
+    const float4* acc = reinterpret_cast<const float4*>(p.dqacc + e0);
+    uint2* out = reinterpret_cast<uint2*>(p.dq + e0);
+    const int n4 = rows * (HD / 4);
+    if (nacc == 0) {
+      for (int i = tid; i < n4; i += kThreads) out[i] = make_uint2(0u, 0u);
+    } else {
+      // two vectors per thread and pass: all loads first, then the sums
+      for (int i0 = tid; i0 < n4; i0 += 2 * kThreads) {
+        float4 w[2][kAccWays];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int m = 0; m < kAccWays; ++m)
+            if (m < nacc && i0 + h * kThreads < n4)
+              w[h][m] = __ldcg(acc + i0 + h * kThreads + m * stride4);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = i0 + h * kThreads;
+          if (i >= n4) break;
+          float4 v = w[h][0];
+#pragma unroll
+          for (int m = 1; m < kAccWays; ++m) {
+            if (m < nacc) {
+              v.x += w[h][m].x; v.y += w[h][m].y; v.z += w[h][m].z; v.w += w[h][m].w;
+            }
+          }
+          out[i] = make_uint2(pack_bf16x2(p.scale * v.x, p.scale * v.y),
+                              pack_bf16x2(p.scale * v.z, p.scale * v.w));
+        }
+      }
+    }
+    __syncthreads();  // misc->conv is rewritten for the next tile
+  }
 }
 
 // kRagged: S is not a multiple of the tile, so the last tile of each head is
@@ -688,6 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  if (p.fuse_convert) tail_convert<HD, kRagged>(p, misc, wc);
 }
 
 }  // namespace

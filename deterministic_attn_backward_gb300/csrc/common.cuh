@@ -19,7 +19,8 @@ struct WsHeader {
   uint32_t status;   // 0 or the first device error
   uint32_t detail;   // where it happened (see kDetail*)
   uint32_t ticket;   // dynamic unit dispatch counter
-  uint32_t pad[61];
+  uint32_t conv_ticket;  // dQ tiles claimed for finalisation in the kernel's tail
+  uint32_t pad[60];
 };
 
 // Detail codes: the high byte says which wait ran out, the rest is context.
@@ -57,6 +58,10 @@ struct BwdParams {
   float scale, scale_log2e;
   unsigned long long timeout_ns;
   int plain_add;                        // ordered schedules: load + add + store instead of red
+  // Ordered schedules: the main kernel also writes dQ = bf16(scale * sum of
+  // the buffers), tile by tile, in its tail (no separate convert pass).
+  int fuse_convert;
+  __nv_bfloat16* dq;                    // [B*H*S, d]
   // Block mask (block != 0): the schedule comes from tables built on the
   // device from the tile flags, shared by all heads.
   int block;

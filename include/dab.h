@@ -103,7 +103,7 @@ dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v,
 
 /* Bytes of device workspace that dab_attn_bwd needs for this problem (0 on
  * invalid arguments).  The workspace holds the status word, the dispatch
- * counter, the semaphores (per 128-row dQ tile: one per eighth of the tile
+ * counters, the semaphores (per 128-row dQ tile: one per eighth of the tile
  * and per accumulation buffer), D and LSE*log2(e) per row, and the float32
  * dQ accumulation buffers [ways][B][H][S][d] (four interleaved buffers for
  * the ordered schedules, one for ATOMIC).  It needs no initialisation: the
@@ -120,9 +120,11 @@ size_t dab_bwd_workspace_size(int B, int H, int S, int d,
  *   2. the persistent main kernel: per KV tile, S, P, dV, dP, dS, dK and the
  *      dQ partial on the tensor cores, then the dQ reduction in the order
  *      `sched` defines (semaphore-ordered, no float atomics, for the three
- *      deterministic schedules);
- *   3. the convert kernel: dQ = bf16(scale * sum of the accumulation
- *      buffers, added in buffer order).
+ *      deterministic schedules), and, for those schedules, in the kernel's
+ *      tail, dQ = bf16(scale * sum of the accumulation buffers, added in
+ *      buffer order) for every 128-row tile once its contributions are in;
+ *   3. for ATOMIC only: the convert kernel, the same dQ formula as a separate
+ *      pass (see DAB_BWD_SEPARATE_CONVERT).
  * The call returns once the kernels are queued.                              */
 dab_status_t dab_attn_bwd(const void* q, const void* k, const void* v,
                           const void* o, const float* lse, const void* dout,
@@ -196,16 +198,23 @@ typedef struct {
  * workspace itself (used to inject faults from the host, e.g. to poison a
  * semaphore and check that the bounded wait reports DAB_ERR_TIMEOUT).       */
 #define DAB_BWD_SKIP_PREPROCESS 0x1u
-/* Skip the convert kernel (dQ is left in the workspace accumulator).        */
+/* Skip the conversion of dQ to bf16, in the main kernel and as a separate
+ * pass (dQ is left in the workspace accumulator).                          */
 #define DAB_BWD_SKIP_CONVERT 0x2u
 /* Skip the main kernel (measurement only: with DAB_BWD_SKIP_PREPROCESS it
- * runs the convert kernel alone, so that its time can be taken; dQ, dK and
- * dV are then not the gradients).                                          */
+ * runs the separate convert pass alone, so that its time can be taken; dQ,
+ * dK and dV are then not the gradients).                                   */
 #define DAB_BWD_SKIP_MAIN 0x4u
 /* Ordered schedules: add each dQ partial to the accumulator with a load from
  * the L2, an add in registers and a store, instead of red.add.f32 in the L2
  * (the same additions in the same order; the default is the red).          */
 #define DAB_BWD_PLAIN_ADD 0x8u
+/* Ordered schedules: convert dQ in a separate pass after the main kernel.
+ * By default the main kernel does it itself: once a CTA has no units left it
+ * converts the dQ tiles whose contributions are all in (bounded waits on the
+ * dQ semaphores), with the same arithmetic as the separate pass, so both
+ * give the same bits.  The atomic schedule always uses the separate pass.  */
+#define DAB_BWD_SEPARATE_CONVERT 0x10u
 
 dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v,
                              const void* o, const float* lse, const void* dout,
