@@ -360,8 +360,11 @@ int dab_dag_simulate_ways(dab_sched_t sched, dab_mask_t mask, int N, int heads,
  * deterministic schedule (SERIAL, DESCENDING_Q or SHIFT) with the smallest
  * makespan in the DAG model of dab_dag_simulate_ways() for B*H heads of
  * S/128 tiles on `ctas` CTAs, with weights fitted to this library's GB300
- * measurements (wr = wc, reducer_depth 1, 4 buffers); ties go to
- * DESCENDING_Q, then SERIAL.  Host only, no CUDA call; -1 on bad arguments.
+ * measurements (wr = wc, reducer_depth 1, 4 buffers).  SHIFT's predicted
+ * makespan is multiplied by 1.025 before the comparison.  This accounts for
+ * its lock-step rings, which the model does not capture; the factor was
+ * fitted to the measured GB300 sweep.  Ties go to DESCENDING_Q, then SERIAL.
+ * Host only, no CUDA call; -1 on bad arguments.
  * Results are cached per (mask, B*H, S, ctas); thread-safe.                 */
 int dab_sched_select(dab_mask_t mask, int B, int H, int S, int ctas);
 
