@@ -77,23 +77,36 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
 
   const int sub = lane / kLanesPerRow;   // row within the warp's group
   const int part = lane % kLanesPerRow;  // 16-byte piece of the row
-  for (long long r0 = gwarp * kRowsPerWarp; r0 < rows; r0 += nwarps * kRowsPerWarp) {
-    const long long row = r0 + sub;
-    float acc = 0.f;
-    if (row < rows) {
-      const uint4 a = reinterpret_cast<const uint4*>(o + row * HD)[part];
-      const uint4 b = reinterpret_cast<const uint4*>(dout + row * HD)[part];
-      acc = dot8_bf16(a, b);
+  // kGroups row groups per warp and pass, all loads issued before the sums
+  constexpr int kGroups = 4;
+  for (long long r0 = gwarp * kRowsPerWarp * kGroups; r0 < rows;
+       r0 += nwarps * kRowsPerWarp * kGroups) {
+    uint4 a[kGroups], b[kGroups];
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      const long long row = r0 + g * kRowsPerWarp + sub;
+      if (row < rows) {
+        a[g] = reinterpret_cast<const uint4*>(o + row * HD)[part];
+        b[g] = reinterpret_cast<const uint4*>(dout + row * HD)[part];
+      } else {
+        a[g] = make_uint4(0u, 0u, 0u, 0u);
+        b[g] = a[g];
+      }
     }
 #pragma unroll
-    for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
-      acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (row < rows && part == 0) {
-      // padded per-head index (rows < 2^31: 32-bit arithmetic)
-      const int ir = (int)row;
-      const int idx = (S_pad == S) ? ir : (ir / S) * S_pad + ir % S;
-      D[idx] = acc;
-      lse2[idx] = lse[row] * kLog2e;
+    for (int g = 0; g < kGroups; ++g) {
+      const long long row = r0 + g * kRowsPerWarp + sub;
+      float acc = dot8_bf16(a[g], b[g]);
+#pragma unroll
+      for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (row < rows && part == 0) {
+        // padded per-head index (rows < 2^31: 32-bit arithmetic)
+        const int ir = (int)row;
+        const int idx = (S_pad == S) ? ir : (ir / S) * S_pad + ir % S;
+        D[idx] = acc;
+        lse2[idx] = lse[row] * kLog2e;
+      }
     }
   }
 }
