@@ -39,8 +39,8 @@ DET_SCHEDS = ("serial", "descending_q", "shift")
 # number of heads, so x2), keyed by the SHA-1 of the kernel source it was
 # taken on.  Reported only while the source is unchanged.
 TRAFFIC_CAPTURES = {
-    # causal 389.5 + 349.8 MB, full 399.4 + 369.1 MB: mean of the masks, x2
-    "d492d236bfb3ebce3ff35f94bca783af19d0f5af": 2 * ((389.5 + 349.8) + (399.4 + 369.1)) / 2 * 1e6,
+    # causal 390.2 + 350.2 MB, full 398.3 + 366.3 MB: mean of the masks, x2
+    "8ad21261094c8ef57599822e43538f7d083882b5": 2 * ((390.2 + 350.2) + (398.3 + 366.3)) / 2 * 1e6,
 }
 MASKS = ("causal", "full")
 

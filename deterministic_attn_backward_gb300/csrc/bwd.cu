@@ -16,8 +16,11 @@
 // written once at its end.  The dQ partial is added to an f32 accumulator in
 // global memory by the reducer warps: for the deterministic schedules in the
 // fixed order rank(i, j) (technical summary section 1: a fixed accumulation
-// order for dQ), waiting on per-(head, Q tile, eighth) semaphores with acquire loads
-// and publishing with a release store; for ATOMIC with unordered float adds.
+// order for dQ), waiting on per-(head, Q tile, eighth, buffer) semaphores
+// with acquire loads and publishing with a release store; for ATOMIC with
+// unordered float adds.  For the deterministic schedules the same kernel then
+// converts dQ to bf16 in its tail: a CTA without units left converts the dQ
+// tiles whose semaphores show every contribution in.
 //
 // Warp roles (20 warps):
 //   warp 0      TMA producer (K_i, V_i per chain; Q_j, dO_j, LSE_j, D_j per
@@ -26,6 +29,7 @@
 //   warps 4-11  softmax / dS, two warpgroups of 64 Q columns each (thread =
 //               KV row), and the chain epilogue (dV by one, dK by the other)
 //   warps 12-19 dQ reducer, one eighth of the dQ tile and one semaphore each
+//   all warps   after the last unit: the dQ convert of finished tiles
 // Every wait is bounded: on expiry the kernel records DAB_ERR_TIMEOUT in the
 // workspace and every role drains and returns.
 #include <cuda.h>

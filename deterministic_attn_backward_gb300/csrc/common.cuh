@@ -35,7 +35,7 @@ constexpr int kTile = 128;  // rows of a KV tile and of a Q tile
 
 // The ordered schedules accumulate dQ in kAccWays interleaved f32 buffers:
 // the partial of rank r goes to buffer r mod kAccWays, in rank order within
-// the buffer, and the convert kernel adds the buffers in index order.  A
+// the buffer, and the dQ convert adds the buffers in index order.  A
 // contributor then waits for rank r - kAccWays instead of r - 1, which hides
 // the latency of the cross-SM hand-off; the summation order stays fixed.
 constexpr int kAccWays = 4;
