@@ -288,6 +288,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     barrier()
     e2e_ms = max_over_ranks(c0.elapsed_time(c1), world, dev) / e2e_steps
     check()
+    for m in MASKS:
+        st = dab.check_status(host_ws[m])
+        if st != 0:
+            raise RuntimeError(f"device status {st} (host path, {m})")
     h2d = sum(t.numel() * t.element_size() for m in MASKS for t in host_in[m])
     d2h = sum(t.numel() * t.element_size() for m in MASKS for t in host_out[m])
 

@@ -27,6 +27,7 @@ DAB_BWD_SKIP_CONVERT = 0x2
 DAB_BWD_SKIP_MAIN = 0x4
 DAB_BWD_PLAIN_ADD = 0x8
 DAB_BWD_SEPARATE_CONVERT = 0x10
+DAB_BWD_SHARE_GPU = 0x20
 
 EXPORTED = (
     "dab_attn_fwd", "dab_bwd_workspace_size", "dab_attn_bwd", "dab_check_status",

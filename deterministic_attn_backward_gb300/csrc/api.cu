@@ -428,7 +428,8 @@ static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const 
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident together
-  attr[0].val.cooperative = 1;
+  attr[0].val.cooperative =
+      ((flags & DAB_BWD_SHARE_GPU) && !dab::static_dispatch((int)sched)) ? 0 : 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {&p};

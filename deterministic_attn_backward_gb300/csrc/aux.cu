@@ -152,6 +152,23 @@ __global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__
   }
 }
 
+// The first device error among `n` (status, detail) pairs, written to the
+// header `hdr` (status 0 when every pair is 0).  One thread: n is the number
+// of head groups of a host-buffer call.
+__global__ void status_collect_kernel(const uint32_t* __restrict__ slots, int n,
+                                      WsHeader* __restrict__ hdr) {
+  uint32_t st = 0u, det = 0u;
+  for (int i = 0; i < n; ++i) {
+    if (slots[2 * i] != 0u) {
+      st = slots[2 * i];
+      det = slots[2 * i + 1];
+      break;
+    }
+  }
+  hdr->status = st;
+  hdr->detail = det;
+}
+
 // Schedule tables of a block mask (one CTA): for each KV tile i its visible Q
 // tiles in visit order (ascending, or descending for DESCENDING_Q) and their
 // number; for each Q tile j the rank of each visible KV tile in ascending KV
@@ -203,6 +220,11 @@ cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const flo
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, D, lse2,
         sem, n_sem, hdr, z, nv, BH, S, S_pad);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_status_collect(const uint32_t* slots, int n, void* hdr, cudaStream_t stream) {
+  status_collect_kernel<<<1, 1, 0, stream>>>(slots, n, static_cast<WsHeader*>(hdr));
   return cudaGetLastError();
 }
 

@@ -4,12 +4,16 @@
 // The heads are split into chunks of consecutive (b, h) heads.  On two copy
 // streams owned by the library, the inputs of every chunk are copied to the
 // device back to back, and the gradients of chunk c are copied back while
-// chunk c+1 is computed; the backward of each chunk runs on the caller's
-// stream as an ordinary dab_attn_bwd call on that range of heads (B = 1,
-// H = heads in the chunk), so every chunk computes exactly what the whole
-// call would for those heads.  Events order the three streams: the copies
-// start after the work already queued on the caller's stream, and the
-// caller's stream waits for the last copy back.
+// later chunks are computed.  The backward of each chunk is an ordinary
+// dab_attn_bwd_ex call on that range of heads (B = 1, H = heads in the
+// chunk), so every chunk computes exactly what the whole call would for those
+// heads.  Even chunks run on the caller's stream and odd chunks on a third
+// library stream, each stream with its own backward workspace, and the main
+// kernel is launched with DAB_BWD_SHARE_GPU: the next chunk's CTAs start on
+// the SMs that the current chunk's last, partly filled wave leaves idle.
+// Events order the streams: everything starts after the work already queued
+// on the caller's stream, and the caller's stream waits for the last copy
+// back (which itself waits for every chunk's computation).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -18,13 +22,17 @@
 
 #include "dab.h"
 
+namespace dab {
+cudaError_t launch_status_collect(const uint32_t* slots, int n, void* hdr, cudaStream_t stream);
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultChunks = 8;
 
 struct CopyStreams {
-  cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t in = nullptr, out = nullptr, comp = nullptr;  // comp: odd chunks
 };
 std::mutex g_mu;
 CopyStreams g_streams[kMaxDevices];
@@ -36,12 +44,16 @@ bool copy_streams(CopyStreams* cs) {
   std::lock_guard<std::mutex> lock(g_mu);
   CopyStreams& s = g_streams[dev];
   if (s.in == nullptr) {
-    if (cudaStreamCreateWithFlags(&s.in, cudaStreamNonBlocking) != cudaSuccess) return false;
-    if (cudaStreamCreateWithFlags(&s.out, cudaStreamNonBlocking) != cudaSuccess) {
-      cudaStreamDestroy(s.in);
-      s.in = nullptr;
-      return false;
+    cudaStream_t st[3] = {nullptr, nullptr, nullptr};
+    for (int i = 0; i < 3; ++i) {
+      if (cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking) != cudaSuccess) {
+        for (int j = 0; j < i; ++j) cudaStreamDestroy(st[j]);
+        return false;
+      }
     }
+    s.in = st[0];
+    s.out = st[1];
+    s.comp = st[2];
   }
   *cs = s;
   return true;
@@ -49,10 +61,13 @@ bool copy_streams(CopyStreams* cs) {
 
 size_t round_up(size_t x) { return (x + 255) / 256 * 256; }
 
-// Device workspace of the host path: copies of the inputs and outputs, then
-// the backward workspace of the largest chunk.
+// Device workspace of the host path: a status header (the first device
+// error of any chunk, collected at the end of the call, as dab_check_status
+// reads it) and one (status, detail) slot per chunk, copies of the inputs
+// and outputs, then the backward workspaces of the largest chunk, one per
+// compute stream.
 struct HostLayout {
-  size_t q, k, v, o, dout, lse, dq, dk, dv, ws, ws_bytes, total;
+  size_t slots, q, k, v, o, dout, lse, dq, dk, dv, ws[2], ws_bytes, total;
   int chunks, per_chunk;
 };
 
@@ -67,7 +82,8 @@ bool host_layout(int B, int H, int S, int d, dab_mask_t mask, dab_sched_t sched,
   L->ws_bytes = dab_bwd_workspace_size(1, L->per_chunk, S, d, mask, sched);
   if (L->ws_bytes == 0 || dab_bwd_workspace_size(B, H, S, d, mask, sched) == 0) return false;
   const size_t t = round_up((size_t)bh * S * d * 2), r = round_up((size_t)bh * S * 4);
-  size_t off = 0;
+  L->slots = 256;  // after the status header at offset 0
+  size_t off = L->slots + round_up((size_t)L->chunks * 8);
   for (size_t* f : {&L->q, &L->k, &L->v, &L->o, &L->dout}) {
     *f = off;
     off += t;
@@ -78,8 +94,9 @@ bool host_layout(int B, int H, int S, int d, dab_mask_t mask, dab_sched_t sched,
     *f = off;
     off += t;
   }
-  L->ws = off;
-  L->total = off + round_up(L->ws_bytes);
+  L->ws[0] = off;
+  L->ws[1] = off + round_up(L->ws_bytes);
+  L->total = L->ws[1] + (L->chunks > 1 ? round_up(L->ws_bytes) : 0);
   return true;
 }
 
@@ -134,9 +151,9 @@ extern "C" dab_status_t dab_attn_bwd_host(const void* q, const void* k, const vo
     return e == cudaSuccess;
   };
   const long long bh = (long long)B * H;
-  // copies start after what is already queued on the caller's stream
+  // everything starts after what is already queued on the caller's stream
   if (ok(cudaEventRecord(start, stream)) && ok(cudaStreamWaitEvent(cs.in, start, 0)) &&
-      ok(cudaStreamWaitEvent(cs.out, start, 0))) {
+      ok(cudaStreamWaitEvent(cs.out, start, 0)) && ok(cudaStreamWaitEvent(cs.comp, start, 0))) {
     for (int c = 0; c < L.chunks && st == DAB_OK; ++c) {  // all inputs, back to back
       const long long h0 = (long long)c * L.per_chunk;
       const long long nh = (h0 + L.per_chunk <= bh) ? L.per_chunk : bh - h0;
@@ -147,28 +164,41 @@ extern "C" dab_status_t dab_attn_bwd_host(const void* q, const void* k, const vo
                          nh * head_r, cudaMemcpyHostToDevice, cs.in));
       ok(cudaEventRecord(ev[c], cs.in));
     }
+    dab_bwd_opts_t opts;
+    opts.spin_timeout_ns = 0;
+    opts.flags = DAB_BWD_SHARE_GPU;
+    opts.grid = 0;
     for (int c = 0; c < L.chunks && st == DAB_OK; ++c) {  // compute chunk c, then copy it back
       const long long h0 = (long long)c * L.per_chunk;
       const long long nh = (h0 + L.per_chunk <= bh) ? L.per_chunk : bh - h0;
-      if (!ok(cudaStreamWaitEvent(stream, ev[c], 0))) break;
+      cudaStream_t cstream = (c % 2 == 0) ? stream : cs.comp;
+      if (!ok(cudaStreamWaitEvent(cstream, ev[c], 0))) break;
       auto dp = [&](size_t off) { return static_cast<void*>(w + off + h0 * head_t); };
-      const dab_status_t r =
-          dab_attn_bwd(dp(L.q), dp(L.k), dp(L.v), dp(L.o), reinterpret_cast<const float*>(w + L.lse + h0 * head_r),
-                       dp(L.dout), dp(L.dq), dp(L.dk), dp(L.dv), 1, (int)nh, S, d, scale, mask, sched,
-                       w + L.ws, L.ws_bytes, stream);
+      const dab_status_t r = dab_attn_bwd_ex(
+          dp(L.q), dp(L.k), dp(L.v), dp(L.o), reinterpret_cast<const float*>(w + L.lse + h0 * head_r),
+          dp(L.dout), dp(L.dq), dp(L.dk), dp(L.dv), 1, (int)nh, S, d, scale, mask, sched,
+          w + L.ws[c % 2], L.ws_bytes, cstream, &opts);
       if (r != DAB_OK) {
         st = r;
         break;
       }
-      if (!ok(cudaEventRecord(ev[L.chunks + c], stream)) ||
+      // this chunk's status and detail words, before its workspace is reused
+      if (!ok(cudaMemcpyAsync(w + L.slots + 8 * (size_t)c, w + L.ws[c % 2], 8,
+                              cudaMemcpyDeviceToDevice, cstream)))
+        break;
+      if (!ok(cudaEventRecord(ev[L.chunks + c], cstream)) ||
           !ok(cudaStreamWaitEvent(cs.out, ev[L.chunks + c], 0)))
         break;
       for (int i = 0; i < 3; ++i)
         ok(cudaMemcpyAsync(static_cast<uint8_t*>(hout[i]) + h0 * head_t, w + dout_off[i] + h0 * head_t,
                            nh * head_t, cudaMemcpyDeviceToHost, cs.out));
     }
-    // the caller's stream continues once everything has been copied back
-    if (ok(cudaEventRecord(done, cs.out))) ok(cudaStreamWaitEvent(stream, done, 0));
+    // the caller's stream continues once everything has been copied back;
+    // then the first device error of any chunk goes to the status header
+    if (ok(cudaEventRecord(done, cs.out)) && ok(cudaStreamWaitEvent(stream, done, 0)) &&
+        st == DAB_OK)
+      ok(dab::launch_status_collect(reinterpret_cast<const uint32_t*>(w + L.slots), L.chunks, w,
+                                    stream));
   }
   for (auto& e : ev) cudaEventDestroy(e);  // released once the work using them completes
   return st;

@@ -215,6 +215,14 @@ typedef struct {
  * dQ semaphores), with the same arithmetic as the separate pass, so both
  * give the same bits.  The atomic schedule always uses the separate pass.  */
 #define DAB_BWD_SEPARATE_CONVERT 0x10u
+/* Let the main kernel share the GPU: launch it without the cooperative
+ * attribute when the schedule hands out units dynamically (every schedule but
+ * SHIFT, whose statically placed gangs must be resident together), so that
+ * its CTAs can start on SMs as other kernels release them.  The waits of
+ * those schedules only point at units that running CTAs have claimed, so the
+ * kernel completes whatever else occupies the GPU.  Same results.  The
+ * host-buffer path uses it to overlap the kernels of consecutive chunks.   */
+#define DAB_BWD_SHARE_GPU 0x20u
 
 dab_status_t dab_attn_bwd_ex(const void* q, const void* k, const void* v,
                              const void* o, const float* lse, const void* dout,
@@ -292,17 +300,21 @@ dab_status_t dab_attn_bwd_noalloc(const void* q, const void* k, const void* v,
  * (cudaHostAlloc / cudaHostRegister), otherwise the copies are synchronous.
  * The heads are split into `chunks` groups of consecutive (b, h) heads (0 =
  * the default, 8; at most B*H): the inputs of all groups are copied in back
- * to back on a library-owned stream, each group's backward runs on `stream`
- * as dab_attn_bwd on that range of heads (so its results are those of
+ * to back on a library-owned stream, each group's backward runs as
+ * dab_attn_bwd_ex on that range of heads (so its results are those of
  * dab_attn_bwd for an explicit schedule; DAB_SCHED_AUTO picks per group
- * shape), and each group's gradients are copied back on a second
- * library-owned stream while the next group computes.  Everything starts
- * after the work already queued on `stream`, and `stream` waits for the last
- * copy back: synchronise `stream` before reading dq, dk, dv or reusing the
- * inputs.  dev_ws: device memory of dab_bwd_host_workspace_size() bytes,
- * 256-byte aligned, caller-owned (copies of inputs and outputs, and the
- * backward workspace of one group).  Errors as dab_attn_bwd; on an error
- * after the first group was queued, earlier groups may still complete.      */
+ * shape) with DAB_BWD_SHARE_GPU, even groups on `stream` and odd groups on a
+ * second library-owned stream (consecutive groups overlap on the GPU), and
+ * each group's gradients are copied back on a third library-owned stream
+ * while later groups compute.  Everything starts after the work already
+ * queued on `stream`, and `stream` waits for the last copy back: synchronise
+ * `stream` before reading dq, dk, dv or reusing the inputs.  dev_ws: device
+ * memory of dab_bwd_host_workspace_size() bytes, 256-byte aligned,
+ * caller-owned (a status header, copies of inputs and outputs, and two
+ * backward workspaces of one group); after the call, dab_check_status(dev_ws,
+ * stream) reports the first device error of any group.  Errors as
+ * dab_attn_bwd; on an error after the first group was queued, earlier groups
+ * may still complete.                                                        */
 size_t dab_bwd_host_workspace_size(int B, int H, int S, int d, dab_mask_t mask,
                                    dab_sched_t sched, int chunks);
 
