@@ -143,6 +143,14 @@ dab_status_t check_shape(int B, int H, int S, int d) {
 
 bool empty_problem(int B, int H, int S) { return (long long)B * H * S == 0; }
 
+// An empty backward launches no kernel; it still clears the status and detail
+// words of a workspace it is given, so that dab_check_status reports this call.
+dab_status_t clear_status(void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (workspace == nullptr || !aligned16(workspace) || ws_bytes < 8) return DAB_OK;
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, 8, stream);
+  return e == cudaSuccess ? DAB_OK : cuda_fail(e, "status reset");
+}
+
 int tiles_of(int S) { return (S + 127) / 128; }
 
 dab_status_t check_enums(dab_mask_t mask, dab_sched_t sched) {
@@ -331,7 +339,7 @@ static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const 
                              void* workspace, size_t ws_bytes, cudaStream_t stream,
                              const dab_bwd_opts_t* opts, const uint8_t* tiles) {
   if (check_shape(B, H, S, d) != DAB_OK || check_enums_auto(mask, sched) != DAB_OK) return DAB_ERR_INVALID_ARG;
-  if (empty_problem(B, H, S)) return DAB_OK;
+  if (empty_problem(B, H, S)) return clear_status(workspace, ws_bytes, stream);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return DAB_ERR_INVALID_ARG;

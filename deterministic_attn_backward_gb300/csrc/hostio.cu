@@ -116,8 +116,14 @@ extern "C" dab_status_t dab_attn_bwd_host(const void* q, const void* k, const vo
                                           float scale, dab_mask_t mask, dab_sched_t sched,
                                           void* dev_ws, size_t dev_ws_bytes, int chunks,
                                           cudaStream_t stream) {
-  if (B >= 0 && H >= 0 && S >= 0 && (long long)B * H * S == 0)  // empty problem: nothing to do
-    return dab_bwd_workspace_size(B, H, S, d, mask, sched) ? DAB_OK : DAB_ERR_INVALID_ARG;
+  if (B >= 0 && H >= 0 && S >= 0 && (long long)B * H * S == 0) {  // empty problem: no kernel
+    if (dab_bwd_workspace_size(B, H, S, d, mask, sched) == 0) return DAB_ERR_INVALID_ARG;
+    // the status header still reports this call
+    if (dev_ws != nullptr && (reinterpret_cast<uintptr_t>(dev_ws) & 15u) == 0 && dev_ws_bytes >= 8 &&
+        cudaMemsetAsync(dev_ws, 0, 8, stream) != cudaSuccess)
+      return DAB_ERR_CUDA;
+    return DAB_OK;
+  }
   HostLayout L;
   if (!host_layout(B, H, S, d, mask, sched, chunks, &L)) return DAB_ERR_INVALID_ARG;
   for (const void* p : {q, k, v, o, static_cast<const void*>(lse), dout,

@@ -21,7 +21,8 @@
  *            sequences have the same length S.
  *   Shapes   d must be 64 or 128; S >= 0, any length (the last 128-row tile
  *            of a head may be partial); B, H >= 0; B*H*ceil(S/128)*128 < 2^31.
- *            A problem with B, H or S zero is empty: DAB_OK, nothing runs.
+ *            A problem with B, H or S zero is empty: DAB_OK, no kernel runs
+ *            (a backward call given a workspace clears its status word).
  *   Mask     DAB_MASK_CAUSAL hides key c from query r when c > r (the diagonal
  *            is visible, so no query row is empty).
  *   Memory   Every pointer is a device pointer, allocated and owned by the

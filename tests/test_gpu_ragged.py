@@ -67,7 +67,13 @@ def test_empty_problems(shape):
     o, lse = dab.attn_fwd(z.cuda(), z.cuda(), z.cuda(), "causal")
     assert o.shape == shape and lse.shape == shape[:3]
     for sched in ("serial", "shift", "atomic"):
-        grads = dab.attn_bwd(z.cuda(), z.cuda(), z.cuda(), o, lse, z.cuda(), "causal", sched)
+        ws = dab.new_workspace(B, H, S, d, "causal", sched)
+        ws.fill_(0xFF)  # an empty call launches no kernel but clears the status word
+        grads = dab.attn_bwd(z.cuda(), z.cuda(), z.cuda(), o, lse, z.cuda(), "causal", sched, workspace=ws)
         assert all(g.shape == shape for g in grads)
-    grads = dab.attn_bwd(z, z, z, o.cpu(), lse.cpu(), z, "full", "serial")
+        assert dab.check_status(ws) == 0
+    hws = dab.new_host_workspace(B, H, S, d, "full", "serial")
+    hws.fill_(0xFF)
+    grads = dab.attn_bwd(z, z, z, o.cpu(), lse.cpu(), z, "full", "serial", workspace=hws)
     assert all(g.shape == shape for g in grads)
+    assert dab.check_status(hws) == 0
