@@ -1,0 +1,36 @@
+"""Bitwise run-to-run reproducibility at the full measurement sizes, in the
+benchmark's launch configuration: 20 runs of every deterministic schedule
+and both masks at B=2, H=16, S=8192, d=128 and at B=1, H=32, S=16384, d=128
+(the longest reduction chains), each run compared with the first on the
+device."""
+import pytest
+import torch
+
+import deterministic_attn_backward_gb300 as dab
+from deterministic_attn_backward_gb300 import inputs
+
+RUNS = 20
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape,seed,qk_scale", [((2, 16, 8192, 128), 2, 0.5),
+                                                 ((1, 32, 16384, 128), 3, 1.0)])
+def test_full_size_bitwise_repeatable(shape, seed, qk_scale):
+    B, H, S, d = shape
+    q, k, v, do = (t.cuda() for t in inputs.make_qkvdo(B, H, S, d, seed, qk_scale))
+    ws = dab.new_workspace(B, H, S, d, "full", "serial")   # the largest workspace
+    out = tuple(torch.empty_like(q) for _ in range(3))
+    for mask in ("causal", "full"):
+        o, lse = dab.attn_fwd(q, k, v, mask)
+        for sched in ("serial", "descending_q", "shift"):
+            if sched == "serial" and mask == "causal" and S > 8192:
+                continue  # the slowest combination; covered at S = 8192
+            first = None
+            for _ in range(RUNS):
+                dab.attn_bwd(q, k, v, o, lse, do, mask, sched, workspace=ws, out=out)
+                if first is None:
+                    first = tuple(t.clone() for t in out)
+                else:
+                    for a, b in zip(out, first):
+                        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (mask, sched)
+            assert dab.check_status(ws) == 0
