@@ -78,3 +78,22 @@ def test_plain_adds_give_the_red_bits(mask, sched, d):
                          opts=dab.BwdOpts(spin_timeout_ns=0, flags=dab.DAB_BWD_PLAIN_ADD, grid=0))
     for a, b in zip(red, plain):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ["full", "causal"])
+@pytest.mark.parametrize("sched", ["serial", "descending_q", "shift"])
+def test_bits_do_not_depend_on_the_grid(mask, sched):
+    """The reduction order is fixed by the schedule's ranks alone, never by
+    how many CTAs run or which CTA takes which unit."""
+    B, H, S, d = 2, 3, 2048, 128          # N = 16: shift gangs of 16 (full) / 8 (causal)
+    q, k, v, do = (t.cuda() for t in case(B, H, S, d, 12))
+    o, lse = dab.attn_fwd(q, k, v, mask)
+    base = dab.attn_bwd(q, k, v, o, lse, do, mask, sched)
+    for grid in (64, 37, 16):
+        ws = dab.new_workspace(B, H, S, d, mask, sched)
+        got = dab.attn_bwd(q, k, v, o, lse, do, mask, sched, workspace=ws,
+                           opts=dab.BwdOpts(spin_timeout_ns=0, flags=0, grid=grid))
+        assert dab.check_status(ws) == 0
+        for a, b in zip(got, base):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), grid
