@@ -241,6 +241,24 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     # kernel's tail) with the main kernel skipped, on the causal workspace
     side = side_kernels(dab, qd, kd, vd, dod, fwd["causal"], "causal", step_scheds["causal"],
                         ws["causal"], outs["causal"], stream, ev)
+    # the forward that produces O and LSE (the path's prerequisite, not part
+    # of a step): CUDA events around each call, median of 5 after 2 warm-up;
+    # algorithmic FLOPs 4*B*H*S^2*d (two products), half for causal
+    fwd_t = {}
+    for m in MASKS:
+        ts = []
+        for it in range(7):
+            a, b_ = ev(), ev()
+            a.record(stream)
+            dab.attn_fwd(qd, kd, vd, m)
+            b_.record(stream)
+            b_.synchronize()
+            if it >= 2:
+                ts.append(a.elapsed_time(b_))
+        ms_f = statistics.median(ts)
+        fl = 0.4 * flops(m)
+        fwd_t[m] = {"ms": round(ms_f, 4), "tflops": round(fl / ms_f / 1e9, 1)}
+    side["forward"] = fwd_t
     own_peak = dab.mma_peak(iters=20000)
     check()
 
