@@ -283,7 +283,7 @@ static dab_status_t fwd_impl(const void* q, const void* k, const void* v, void* 
   p.tiles = tiles;
   dab::WsHeader* hdr = static_cast<dab::WsHeader*>(workspace);
   if (hdr != nullptr && cudaMemsetAsync(hdr, 0, 16, stream) != cudaSuccess) return DAB_ERR_CUDA;
-  const dim3 grid((unsigned)(p.BH * p.N)), block(192);
+  const dim3 grid((unsigned)(p.BH * p.N)), block(384);
   void* args[] = {&p, &hdr};
   cudaError_t e;
   if (d == 128)
