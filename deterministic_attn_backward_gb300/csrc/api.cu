@@ -19,6 +19,7 @@ namespace dab {
 // kernels (bwd.cu, fwd.cu, aux.cu, selftest.cu)
 template <int HD> int bwd_smem_bytes();
 template <int HD> const void* bwd_kernel_ptr(bool ragged);
+int fwd_threads();
 template <int HD> int fwd_smem_bytes();
 template <int HD> const void* fwd_kernel_ptr();
 template <int HD> int selftest_smem_bytes();
@@ -283,7 +284,7 @@ static dab_status_t fwd_impl(const void* q, const void* k, const void* v, void* 
   p.tiles = tiles;
   dab::WsHeader* hdr = static_cast<dab::WsHeader*>(workspace);
   if (hdr != nullptr && cudaMemsetAsync(hdr, 0, 16, stream) != cudaSuccess) return DAB_ERR_CUDA;
-  const dim3 grid((unsigned)(p.BH * p.N)), block(384);
+  const dim3 grid((unsigned)(p.BH * p.N)), block((unsigned)dab::fwd_threads());
   void* args[] = {&p, &hdr};
   cudaError_t e;
   if (d == 128)

@@ -31,6 +31,10 @@ namespace {
 
 constexpr int kFwdThreads = 384;
 constexpr int kFwdSoftmaxWarp0 = 4;  // warps 4-7: key columns 0-63, 8-11: 64-127
+constexpr int kFwdSoftmaxWarps = 8;
+// The barrier counts (s_free, p_full) and the named barrier of the (max, sum)
+// combine expect exactly these warps: the block must hold all of them.
+static_assert(kFwdThreads == 32 * (kFwdSoftmaxWarp0 + kFwdSoftmaxWarps), "forward warp roles");
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int HD>
@@ -94,8 +98,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 8);
-      mbar_init(&bars->p_full[s], 8);
+      mbar_init(&bars->s_free[s], kFwdSoftmaxWarps);
+      mbar_init(&bars->p_full[s], kFwdSoftmaxWarps);
       mbar_init(&bars->o_done[s], 1);
     }
     mbar_init(&bars->o_full, 1);
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     // Combine the two warpgroups' (max, sum) of each row.  Every softmax warp
     // reaches this barrier, also after a failed wait.
     stat[h * 128 + r] = make_float2(m, l);
-    named_bar_sync(1, 256);
+    named_bar_sync(1, 32 * kFwdSoftmaxWarps);
     const float2 s0 = stat[r], s1 = stat[128 + r];
     const float mt = fmaxf(s0.x, s1.x);
     float lse2 = -INFINITY;
@@ -344,6 +348,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 }
 
 }  // namespace
+
+int fwd_threads() { return kFwdThreads; }
 
 template <int HD>
 int fwd_smem_bytes() {
