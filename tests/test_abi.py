@@ -130,3 +130,18 @@ def test_bad_arguments_rejected_without_touching_the_device(lib):
     assert lib.dab_mma_peak(0, p, None) == 1
     assert lib.dab_mma_peak(1 << 23, p, None) == 1
     assert lib.dab_mma_peak(1000, ctypes.c_void_p(17), None) == 1
+
+
+def test_host_workspace_holds_two_group_workspaces(lib):
+    """The host-buffer path: a status header and per-group slots, device
+    copies of the nine tensors, and one backward workspace per compute
+    stream (two once there are at least two groups)."""
+    rnd = lambda x: (x + 255) // 256 * 256
+    B, H, S, d = 2, 3, 640, 128
+    bh = B * H
+    copies = 8 * rnd(bh * S * d * 2) + rnd(bh * S * 4)
+    for chunks, per in ((1, 6), (2, 3), (6, 1)):
+        group_ws = rnd(lib.dab_bwd_workspace_size(1, per, S, d, 0, 1))
+        size = lib.dab_bwd_host_workspace_size(B, H, S, d, 0, 1, chunks)
+        want = 256 + rnd(8 * chunks) + copies + (2 if chunks > 1 else 1) * group_ws
+        assert size == want, (chunks, size, want)
