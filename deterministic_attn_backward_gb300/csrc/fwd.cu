@@ -248,13 +248,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         tmem_ld32(tbase + lane_off + C::kColS + 128u * b + 64 * h + 32 * ch, v);
         float x[32];
         float cmax = -INFINITY;
+        // masks apply only on the causal diagonal tile and a partial last tile
+        const bool masked = (causal && c == qi) || (c + 1) * kTile > p.S;
+        if (masked) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = 64 * h + 32 * ch + e;
-          x[e] = __uint_as_float(v[e]) * p.scale_log2e;
-          if (causal && c == qi && col > r) x[e] = -INFINITY;
-          if (c * kTile + col >= p.S) x[e] = -INFINITY;   // past the end of a partial last tile
-          cmax = fmaxf(cmax, x[e]);
+          for (int e = 0; e < 32; ++e) {
+            const int col = 64 * h + 32 * ch + e;
+            x[e] = __uint_as_float(v[e]) * p.scale_log2e;
+            if (causal && c == qi && col > r) x[e] = -INFINITY;
+            if (c * kTile + col >= p.S) x[e] = -INFINITY;   // past the end of a partial last tile
+            cmax = fmaxf(cmax, x[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            x[e] = __uint_as_float(v[e]) * p.scale_log2e;
+            cmax = fmaxf(cmax, x[e]);
+          }
         }
         // A half row may have seen no visible key yet (its keys all masked):
         // then the sum stays exactly 0 (no -inf - -inf).
@@ -293,17 +303,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         uint32_t v[32];
         tmem_ld32(tS + 32 * ch, v);
         uint32_t w16[16];
+        const bool masked = (causal && c == qi) || (c + 1) * kTile > p.S;
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int col = 64 * h + 32 * ch + e;
           float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2e, -lse2));
           float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2e, -lse2));
-          if (causal && c == qi) {
-            if (col > r) p0 = 0.f;
-            if (col + 1 > r) p1 = 0.f;
+          if (masked) {
+            if (causal && c == qi) {
+              if (col > r) p0 = 0.f;
+              if (col + 1 > r) p1 = 0.f;
+            }
+            if (c * kTile + col >= p.S) p0 = 0.f;
+            if (c * kTile + col + 1 >= p.S) p1 = 0.f;
           }
-          if (c * kTile + col >= p.S) p0 = 0.f;
-          if (c * kTile + col + 1 >= p.S) p1 = 0.f;
           w16[e >> 1] = pack_bf16x2(p0, p1);
         }
         // P over the columns this thread has read (packed: 16 words per 32 keys)
