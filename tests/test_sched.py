@@ -249,3 +249,23 @@ def test_sched_select_matches_the_measured_gb300_winners():
     assert dab.sched_select("full", 2, 16, 8192, 152) == "descending_q"
     assert dab.sched_select("full", 4, 16, 2048, 152) == "shift"
     assert dab.sched_select("causal", 4, 16, 2048, 152) == "shift"
+
+
+@pytest.mark.parametrize("sched", ["serial", "descending_q", "shift"])
+@pytest.mark.parametrize("mask", ["full", "causal"])
+@pytest.mark.parametrize("N", [1, 2, 5, 8, 16, 64])
+def test_final_counts_of_the_accumulation_buffers(sched, mask, N):
+    """The main kernel's tail converts dQ tile j once every buffer m < min(c, 4)
+    holds (c - 1 - m) // 4 + 1 contributions (c contributors, rank r going to
+    buffer r mod 4).  Counted here from the schedule's own ranks."""
+    if sched == "shift" and mask == "causal" and N % 2:
+        return
+    W = 4
+    for j in range(N):
+        c = dab.sched_contributors(mask, N, j)
+        assert c == (N if mask == "full" else j + 1)
+        ranks = [dab.sched_rank(sched, mask, N, i, j) for i in range(N)
+                 if mask == "full" or i <= j]
+        assert sorted(ranks) == list(range(c))
+        for m in range(min(c, W)):
+            assert sum(1 for r in ranks if r % W == m) == (c - 1 - m) // W + 1
