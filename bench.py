@@ -34,9 +34,9 @@ SEED, QK_SCALE = 2, 0.5
 ALL_SCHEDS = ("serial", "descending_q", "shift", "atomic")
 DET_SCHEDS = ("serial", "descending_q", "shift")
 
-# DRAM bytes (read + write) of one main-kernel launch of this workload, from an
-# ncu capture (profiles/bwd_main_*.md: B=1 launches, traffic scales with the
-# number of heads, so x2), keyed by the SHA-1 of the kernel source it was
+# DRAM bytes (read + write) of one main-kernel launch of this workload, from
+# ncu captures of B=1 launches of the same kernel (traffic scales with the
+# number of heads, so x2), keyed by the SHA-1 of the kernel source they were
 # taken on.  Reported only while the source is unchanged.
 TRAFFIC_CAPTURES = {
     # causal 390.2 + 350.2 MB, full 398.3 + 366.3 MB: mean of the masks, x2
@@ -190,31 +190,67 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     step()
     check()
 
-    # ---- per-schedule table: device time per call of the whole hot path
+    # ---- per-schedule table: device time per call of the whole hot path;
+    # `main_ms`: the main kernel alone (events around its launch; for the
+    # ordered schedules it includes the dQ convert in its tail, for atomic
+    # the separate convert pass is left out), so that the deterministic and
+    # atomic schedules are also compared on like work; `plain_add`: the
+    # ordered schedules with DAB_BWD_PLAIN_ADD (load + add + store, no float
+    # atomic; same bits as the default red.add.f32)
+    def timed_calls(m, sched, flags=0, reps=10):
+        o_, lse_ = fwd[m]
+        opts_ = dab.BwdOpts(spin_timeout_ns=0, flags=flags, grid=0)
+        for _ in range(3):
+            dab.attn_bwd(qd, kd, vd, o_, lse_, dod, m, sched, workspace=ws[m], out=outs[m], opts=opts_)
+        torch.cuda.synchronize(dev)
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _ in range(reps):
+            dab.attn_bwd(qd, kd, vd, o_, lse_, dod, m, sched, workspace=ws[m], out=outs[m], opts=opts_)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def main_kernel_ms(m, sched, reps=10):
+        o_, lse_ = fwd[m]
+        flags = dab.DAB_BWD_SKIP_PREPROCESS | (dab.DAB_BWD_SKIP_CONVERT if sched == "atomic" else 0)
+        opts_ = dab.BwdOpts(spin_timeout_ns=0, flags=flags, grid=0)
+        tot = 0.0
+        for it in range(reps + 2):
+            dab.bwd_preprocess(o_, lse_, dod, m, sched, ws[m])
+            a, b_ = ev(), ev()
+            a.record(stream)
+            dab.attn_bwd(qd, kd, vd, o_, lse_, dod, m, sched, workspace=ws[m], out=outs[m], opts=opts_)
+            b_.record(stream)
+            b_.synchronize()
+            if it >= 2:
+                tot += a.elapsed_time(b_)
+        return tot / reps
+
     per = {}
     for m in MASKS:
         per[m] = {}
         for sched in ALL_SCHEDS:
-            for _ in range(3):
-                bwd(m, sched)
-            torch.cuda.synchronize(dev)
-            reps = 10
-            e0, e1 = ev(), ev()
-            e0.record(stream)
-            for _ in range(reps):
-                bwd(m, sched)
-            e1.record(stream)
-            e1.synchronize()
-            ms = e0.elapsed_time(e1) / reps
-            per[m][sched] = {"ms": round(ms, 4), "tflops": round(flops(m) / ms / 1e9, 2)}
+            ms = timed_calls(m, sched)
+            mk = main_kernel_ms(m, sched)
+            per[m][sched] = {"ms": round(ms, 4), "tflops": round(flops(m) / ms / 1e9, 2),
+                             "main_ms": round(mk, 4), "main_tflops": round(flops(m) / mk / 1e9, 2)}
+            if sched != "atomic":
+                pm = timed_calls(m, sched, dab.DAB_BWD_PLAIN_ADD)
+                per[m][sched]["plain_add"] = {"ms": round(pm, 4),
+                                              "tflops": round(flops(m) / pm / 1e9, 2),
+                                              "vs_red": round(pm / ms, 4)}
         check()
         # a step runs, per mask, the fastest deterministic schedule
         step_scheds[m] = min(DET_SCHEDS, key=lambda x: per[m][x]["ms"])
         ts, ta = per[m]["serial"]["ms"], per[m]["atomic"]["ms"]
+        ms_, ma = per[m]["serial"]["main_ms"], per[m]["atomic"]["main_ms"]
         for sched in ("descending_q", "shift"):
-            gap = ts - ta
+            gap, gap_m = ts - ta, ms_ - ma
             per[m][sched]["gap_closure"] = (round((ts - per[m][sched]["ms"]) / gap, 3)
                                             if abs(gap) > 1e-9 else None)
+            per[m][sched]["gap_closure_main"] = (round((ms_ - per[m][sched]["main_ms"]) / gap_m, 3)
+                                                 if abs(gap_m) > 1e-9 else None)
 
     # ---- the dominant kernel alone (events around each main-kernel launch,
     # as the step launches it: with the dQ convert in its tail)

@@ -37,7 +37,7 @@ EXPORTED = (
     "dab_dag_simulate_ways", "dab_sched_select", "dab_attn_bwd_host", "dab_bwd_host_workspace_size",
     "dab_attn_fwd_block", "dab_attn_bwd_block", "dab_bwd_block_workspace_size",
     "dab_selftest_mma", "dab_last_error_string", "dab_attn_bwd_noalloc", "dab_mma_peak",
-    "dab_mma_peak_grid",
+    "dab_mma_peak_grid", "dab_noalloc_check_status",
 )
 
 
@@ -124,6 +124,8 @@ def load_library(path: str = LIB_PATH):
     lib.dab_dag_critical_path.restype = ctypes.c_double
     lib.dab_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 4 + [f, i, i, vp]
     lib.dab_attn_bwd_noalloc.restype = i
+    lib.dab_noalloc_check_status.argtypes = [vp]
+    lib.dab_noalloc_check_status.restype = i
     lib.dab_selftest_mma.argtypes = [i] + [vp] * 10
     lib.dab_selftest_mma.restype = i
     lib.dab_mma_peak.argtypes = [i, vp, vp]

@@ -32,7 +32,10 @@ std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Once per device, with that device current: look up the device address of
-// the scratch array.  Returns nullptr if the lookup failed.
+// the scratch array.  Returns nullptr if the lookup failed.  The address is
+// kept for the life of the process; a cudaDeviceReset() unloads the module
+// that holds the array, so this entry point must not be used on a device
+// after it has been reset.
 void* scratch_for_current_device(int* dev_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -47,6 +50,21 @@ void* scratch_for_current_device(int* dev_out) {
 }
 
 }  // namespace
+
+extern "C" dab_status_t dab_noalloc_check_status(cudaStream_t stream) {
+  int dev = -1;
+  void* scratch = scratch_for_current_device(&dev);
+  if (scratch == nullptr) return DAB_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DAB_ERR_CUDA;
+  // The status and detail words head the array (offset 0 of the workspace
+  // layout); copied into host stack memory, nothing is allocated.
+  uint32_t hdr[2] = {0u, 0u};
+  if (cudaMemcpyFromSymbol(hdr, g_scratch, sizeof(hdr), 0, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DAB_ERR_CUDA;
+  if (hdr[0] == 0u) return DAB_OK;
+  if (hdr[0] == DAB_ERR_TIMEOUT || hdr[0] == DAB_ERR_DEVICE_BOUNDS) return (dab_status_t)hdr[0];
+  return DAB_ERR_DEVICE_BOUNDS;
+}
 
 extern "C" dab_status_t dab_attn_bwd_noalloc(const void* q, const void* k, const void* v,
                                              const void* o, const float* lse, const void* dout,

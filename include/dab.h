@@ -26,9 +26,17 @@
  *   Mask     DAB_MASK_CAUSAL hides key c from query r when c > r (the diagonal
  *            is visible, so no query row is empty).
  *   Memory   Every pointer is a device pointer, allocated and owned by the
- *            caller, 16-byte aligned.  The library allocates no device memory
- *            and keeps no state between calls except a per-device cache of
- *            kernel attributes.
+ *            caller, 16-byte aligned (except the host-buffer path,
+ *            dab_attn_bwd_host, whose tensors live in host memory).  The
+ *            library never calls cudaMalloc.  State it keeps between calls:
+ *            a per-device cache of kernel attributes and of the SM count;
+ *            the schedule-selection cache (dab_sched_select); three
+ *            library-owned CUDA streams per device, created on the first
+ *            dab_attn_bwd_host call on that device (its events are created
+ *            and released within each call); and the
+ *            fixed scratch array of dab_attn_bwd_noalloc
+ *            (DAB_NOALLOC_SCRATCH_BYTES of device memory, part of the
+ *            library's image on every GPU that loads it).
  *   Streams  Every call is asynchronous on `stream` and may run concurrently
  *            with calls on other streams that use distinct workspaces.
  *   Errors   Argument errors are returned synchronously and launch nothing.
@@ -120,10 +128,16 @@ size_t dab_bwd_workspace_size(int B, int H, int S, int d,
  *      ATOMIC, zeroing of the dQ accumulator);
  *   2. the persistent main kernel: per KV tile, S, P, dV, dP, dS, dK and the
  *      dQ partial on the tensor cores, then the dQ reduction in the order
- *      `sched` defines (semaphore-ordered, no float atomics, for the three
- *      deterministic schedules), and, for those schedules, in the kernel's
- *      tail, dQ = bf16(scale * sum of the accumulation buffers, added in
- *      buffer order) for every 128-row tile once its contributions are in;
+ *      `sched` defines, and, for the three deterministic schedules, in the
+ *      kernel's tail, dQ = bf16(scale * sum of the accumulation buffers,
+ *      added in buffer order) for every 128-row tile once its contributions
+ *      are in.  The deterministic reduction is semaphore-ordered: a
+ *      contributor adds its partial only once every contributor of lower
+ *      rank in the same buffer has published, so each element receives its
+ *      additions in one fixed order.  By default that addition is a float
+ *      reduction in the L2 (red.add.f32), issued by one contributor at a
+ *      time; DAB_BWD_PLAIN_ADD replaces it with a load, an add in registers
+ *      and a store, which gives the same bits and uses no float atomic;
  *   3. for ATOMIC only: the convert kernel, the same dQ formula as a separate
  *      pass (see DAB_BWD_SEPARATE_CONVERT).
  * The call returns once the kernels are queued.                              */
@@ -208,7 +222,9 @@ typedef struct {
 #define DAB_BWD_SKIP_MAIN 0x4u
 /* Ordered schedules: add each dQ partial to the accumulator with a load from
  * the L2, an add in registers and a store, instead of red.add.f32 in the L2
- * (the same additions in the same order; the default is the red).          */
+ * (the same additions in the same order, so the same bits; no float atomic
+ * is then used anywhere on the deterministic path).  The default is the red,
+ * which is faster.                                                          */
 #define DAB_BWD_PLAIN_ADD 0x8u
 /* Ordered schedules: convert dQ in a separate pass after the main kernel.
  * By default the main kernel does it itself: once a CTA has no units left it
@@ -274,14 +290,16 @@ dab_status_t dab_bwd_workspace_layout(int B, int H, int S, int d,
  *   Set-up   the first call on a device, with that device current, looks up
  *            the array's device address (cudaGetSymbolAddress) and caches
  *            it; make that first call before any stream capture.  A failed
- *            lookup returns DAB_ERR_CUDA.
+ *            lookup returns DAB_ERR_CUDA.  The cached address does not
+ *            survive cudaDeviceReset(): do not use this entry point on a
+ *            device after resetting it.
  *   Sharing  every call on a device uses the same array, which keeps the
  *            last call's contents; each call's first kernel clears what must
  *            start at zero.  Calls whose kernels overlap on the GPU (for
  *            instance on two streams) race on the array: serialise them.
- *   Status   the device status word lives in the array too, so
- *            dab_check_status() cannot be pointed at it; a device-side
- *            timeout leaves the gradients undefined.
+ *   Status   the device status word lives in the array too: read it with
+ *            dab_noalloc_check_status() after the call (a device-side
+ *            timeout leaves the gradients undefined).
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.    */
 #define DAB_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
@@ -291,6 +309,13 @@ dab_status_t dab_attn_bwd_noalloc(const void* q, const void* k, const void* v,
                                   int B, int H, int S, int d, float scale,
                                   dab_mask_t mask, dab_sched_t sched,
                                   cudaStream_t stream);
+
+/* The status of the last dab_attn_bwd_noalloc call on the current device, as
+ * dab_check_status() reports it for a workspace: synchronises `stream`, then
+ * copies the status word out of the library's scratch array into host stack
+ * memory (no allocation).  DAB_OK, DAB_ERR_TIMEOUT, DAB_ERR_DEVICE_BOUNDS, or
+ * DAB_ERR_CUDA if the synchronisation or the copy failed.                   */
+dab_status_t dab_noalloc_check_status(cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* The backward on HOST buffers, with the host<->device copies overlapped with

@@ -1,8 +1,9 @@
 """Bitwise run-to-run reproducibility at the full measurement sizes, in the
 benchmark's launch configuration: 20 runs of every deterministic schedule
-and both masks at B=2, H=16, S=8192, d=128 and at B=1, H=32, S=16384, d=128
-(the longest reduction chains), each run compared with the first on the
-device."""
+and both masks at B=2, H=16, S=8192, d=128, at B=1, H=32, S=16384, d=128
+(the longest reduction chains at d = 128) and at B=2, H=16, S=16384, d=64
+(the d = 64 reducer over chains of 128 tiles), each run compared with the
+first on the device."""
 import pytest
 import torch
 
@@ -14,7 +15,8 @@ RUNS = 20
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("shape,seed,qk_scale", [((2, 16, 8192, 128), 2, 0.5),
-                                                 ((1, 32, 16384, 128), 3, 1.0)])
+                                                 ((1, 32, 16384, 128), 3, 1.0),
+                                                 ((2, 16, 16384, 64), 4, 1.0)])
 def test_full_size_bitwise_repeatable(shape, seed, qk_scale):
     B, H, S, d = shape
     q, k, v, do = (t.cuda() for t in inputs.make_qkvdo(B, H, S, d, seed, qk_scale))

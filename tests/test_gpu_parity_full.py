@@ -27,9 +27,17 @@ CONFIGS = [
     ("b2h16s8192d128", 2, 16, 8192, 128, 2, 0.5, ("causal", "full"),
      ("serial", "descending_q", "shift", "atomic"), ((0, 0), (1, 15))),
     ("b1h32s16384d128", 1, 32, 16384, 128, 3, 1.0, ("full", "causal"),
-     ("descending_q", "shift", "atomic"), ((0, 31),)),
+     ("serial", "descending_q", "shift", "atomic"), ((0, 31),)),
     ("b1h16s32768d128", 1, 16, 32768, 128, 4, 1.0, ("causal", "full"),
      ("descending_q", "shift"), ((0, 7),)),
+    # d = 64 at N = 128 and N = 256 tiles: the full-mask shift in one gang of
+    # 128 and in two groups of 128, the causal symmetric shift with gangs of
+    # 64 and 128 CTAs, and the d = 64 reducer (Q rows on tensor-memory lanes)
+    # over long chains
+    ("b2h16s16384d64", 2, 16, 16384, 64, 4, 1.0, ("full", "causal"),
+     ("serial", "descending_q", "shift", "atomic"), ((1, 15),)),
+    ("b1h16s32768d64", 1, 16, 32768, 64, 4, 1.0, ("causal", "full"),
+     ("serial", "descending_q", "shift", "atomic"), ((0, 3),)),
 ]
 
 

@@ -8,6 +8,11 @@ through the C ABI twice in a row and checks both results against the
 ordinary, workspace-taking entry point, within the tolerance of the parity
 tests; it also checks that a problem too large for the array is refused.
 
+The entry point's status word lives in the library's array, and
+dab_noalloc_check_status() must report each call as clean.  A further test
+checks the one promise of the entry point itself: after a warm-up call, a
+call changes the device's free memory by nothing.
+
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
 """
@@ -34,6 +39,11 @@ def _noalloc(q, k, v, o, lse, do, mask, sched, out):
         MASKS[mask], SCHEDS[sched], ctypes.c_void_p(stream))
 
 
+def _status():
+    lib = dab.load_library()
+    return lib.dab_noalloc_check_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
 def _rel(a, b):
     a, b = a.double(), b.double()
     return ((a - b).abs().max() / b.abs().max()).item()
@@ -57,7 +67,8 @@ def test_noalloc_matches_workspace_entry_point(shape, mask, sched):
         out = tuple(torch.full_like(q, float("nan")) for _ in range(3))
         rc = _noalloc(q, k, v, o, lse, do, mask, sched, out)
         assert rc == 0, dab.STATUS.get(rc, rc)
-        torch.cuda.synchronize()
+        st = _status()
+        assert st == 0, dab.STATUS.get(st, st)
         results.append(out)
     for out in results:
         for got, ref in zip(out, want):
@@ -77,3 +88,21 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     rc = lib.dab_attn_bwd_noalloc(p, p, p, p, p, p, p, p, p, B, H, S, d, ctypes.c_float(0.088),
                                   0, 0, None)
     assert rc == 3  # DAB_ERR_WORKSPACE
+
+
+@pytest.mark.gpu
+def test_noalloc_call_leaves_free_device_memory_unchanged():
+    B, H, S, d = 1, 2, 512, 128
+    q, k, v, do = (t.cuda() for t in case(B, H, S, d, 6))
+    o, lse = dab.attn_fwd(q, k, v, "causal")
+    out = tuple(torch.empty_like(q) for _ in range(3))
+    # warm-up: loads the kernels and looks up the array's address
+    assert _noalloc(q, k, v, o, lse, do, "causal", "descending_q", out) == 0
+    assert _status() == 0
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    assert _noalloc(q, k, v, o, lse, do, "causal", "descending_q", out) == 0
+    assert _status() == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
