@@ -30,9 +30,9 @@ int peak_threads();
 cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const float* lse, float* D,
                               float* lse2, uint32_t* sem, int n_sem, WsHeader* hdr, float* dqacc,
                               long long dq_elems, int BH, int S, int S_pad, int grid, cudaStream_t stream);
-cudaError_t launch_convert(const float* dqacc, void* dq, long long elems, float scale,
-                           long long acc_stride, int ways, int causal, int N, int S, int d, int grid,
-                           const int* count, cudaStream_t stream);
+cudaError_t launch_convert(const float* dqacc, void* dq, int ntiles, float scale, long long acc_stride,
+                           int ways, int causal, int N, int S, int d, int grid, const int* count,
+                           cudaStream_t stream);
 cudaError_t launch_block_tables(const uint8_t* tiles, int N, int causal, int descending,
                                 uint16_t* list, uint16_t* rank, int* nact, int* count,
                                 cudaStream_t stream);
@@ -184,8 +184,8 @@ int acc_ways(dab_sched_t sched) { return sched == DAB_SCHED_ATOMIC ? 1 : dab::kA
 
 bool layout(int B, int H, int S, int d, dab_sched_t sched, dab_ws_layout_t* L) {
   if (check_shape(B, H, S, d) != DAB_OK) return false;
-  const size_t BH = (size_t)B * H, N = (size_t)tiles_of(S), rows = BH * S;
-  const size_t rows_pad = BH * N * 128;  // D and LSE2 per head padded to whole tiles
+  const size_t BH = (size_t)B * H, N = (size_t)tiles_of(S);
+  const size_t rows_pad = BH * N * 128;  // D, LSE2 and dQ per head padded to whole tiles
   const size_t ways = (size_t)acc_ways(sched);
   size_t off = 0;
   L->status = off;
@@ -196,8 +196,8 @@ bool layout(int B, int H, int S, int d, dab_sched_t sched, dab_ws_layout_t* L) {
   off = round_up(off + rows_pad * 4, 256);
   L->lse2 = off;
   off = round_up(off + rows_pad * 4, 256);
-  L->dqacc = off;
-  off = round_up(off + ways * rows * (size_t)d * 4, 256);
+  L->dqacc = off;  // chunk-major tiles, every head padded to whole tiles
+  off = round_up(off + ways * rows_pad * (size_t)d * 4, 256);
   L->total = off;
   return true;
 }
@@ -323,13 +323,14 @@ dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dou
   if (!device_setup(nullptr, &sms)) return DAB_ERR_UNSUPPORTED;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const long long rows = (long long)B * H * S;
+  const long long rows_pad = (long long)B * H * tiles_of(S) * 128;
   const int n_sem = B * H * tiles_of(S) * dab::kSubTiles * acc_ways(sched);
   float* dqacc = (sched == DAB_SCHED_ATOMIC) ? reinterpret_cast<float*>(ws + L.dqacc) : nullptr;
   const int grid = elementwise_grid(sms, rows * (d / 8));
   cudaError_t e = dab::launch_preprocess(
       d, o, dout, lse, reinterpret_cast<float*>(ws + L.D), reinterpret_cast<float*>(ws + L.lse2),
       reinterpret_cast<uint32_t*>(ws + L.sem), n_sem, reinterpret_cast<dab::WsHeader*>(ws + L.status),
-      dqacc, rows * d, B * H, S, tiles_of(S) * 128, grid, stream);
+      dqacc, rows_pad * d, B * H, S, tiles_of(S) * 128, grid, stream);
   return e == cudaSuccess ? DAB_OK : cuda_fail(e, "preprocess launch");
 }
 
@@ -399,7 +400,7 @@ static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const 
   p.D = reinterpret_cast<const float*>(ws + L.D);
   p.dqacc = reinterpret_cast<float*>(ws + L.dqacc);
   p.acc_ways = acc_ways(sched);
-  p.acc_stride = rows * d;
+  p.acc_stride = (long long)B * H * N * 128 * d;  // floats per buffer (padded tiles)
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.sem = reinterpret_cast<uint32_t*>(ws + L.sem);
@@ -451,9 +452,10 @@ static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const 
   }
 
   if (!(flags & DAB_BWD_SKIP_CONVERT) && !p.fuse_convert) {
-    const long long elems = rows * d;
-    e = dab::launch_convert(p.dqacc, dq, elems, scale, p.acc_stride, p.acc_ways,
-                            mask == DAB_MASK_CAUSAL ? 1 : 0, N, S, d, elementwise_grid(sms, elems / 4),
+    const int ntiles = B * H * N;
+    const int cgrid = ntiles < 8 * sms ? ntiles : 8 * sms;
+    e = dab::launch_convert(p.dqacc, dq, ntiles, scale, p.acc_stride, p.acc_ways,
+                            mask == DAB_MASK_CAUSAL ? 1 : 0, N, S, d, cgrid,
                             block ? p.blk_count : nullptr, stream);
     if (e != cudaSuccess) return cuda_fail(e, "convert launch");
   }

@@ -111,44 +111,85 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
   }
 }
 
+// dQ = bf16(scale * sum of the accumulation buffers), tile by tile.  The
+// buffers that received a contribution (min(ways, contributors of the Q
+// tile): N for the full mask, j + 1 for causal, the tables' count under a
+// block mask, 0 -> dQ = 0) are added in index order, times scale, rounded to
+// bf16 (RN-even): the arithmetic of the main kernel's tail, so both give the
+// same bits.  d = 128: row-major accumulator [B*H*S][d], 16-byte vectors.
+// d = 64: chunk-major tiles [d/4][128 rows][4] (every head padded to whole
+// tiles), read 16 bytes per thread over consecutive rows, staged in shared
+// memory and written row by row.
+template <int HD>
 __global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__ acc,
-                                                      uint2* __restrict__ out, long long n_vec4,
+                                                      __nv_bfloat16* __restrict__ dq, int ntiles,
                                                       float scale, long long acc_stride_vec4,
-                                                      int ways, int causal, int N, int S, int d,
+                                                      int ways, int causal, int N, int S,
                                                       const int* __restrict__ count) {
-  const long long n = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec4; i += n) {
-    // buffers that received a contribution: min(ways, contributors of the Q
-    // tile), with N contributors per tile for the full mask, j + 1 for
-    // causal, and the tables' count under a block mask (0: dQ = 0)
+  constexpr int kChunks = HD / 4;
+  constexpr int kRowBytes = HD * 2 + 16;
+  __shared__ __align__(16) uint8_t stage[(HD == 64) ? kTile * kRowBytes : 16];
+  for (int T = blockIdx.x; T < ntiles; T += gridDim.x) {
+    const int bh = T / N, j = T % N;
     int nacc = ways < N ? ways : N;
-    if (count != nullptr || (causal && nacc > 1)) {
-      const long long row = (i * 4) / d;
-      const int j = (int)((row % S) / kTile);
+    if (count != nullptr || causal) {
       const int c = (count != nullptr) ? count[j] : j + 1;
       if (c < nacc) nacc = c;
     }
-    if (nacc == 0) {
-      out[i] = make_uint2(0u, 0u);
-      continue;
-    }
-    // all loads first (at most kAccWays buffers), then the sum in the
-    // fixed order buffer 0, 1, ...
-    float4 w[kAccWays];
+    const int rows = min(kTile, S - j * kTile);
+    if constexpr (HD == 128) {
+      const size_t e0 = ((size_t)bh * S + (size_t)j * kTile) * HD;
+      const float4* a = acc + e0 / 4;
+      uint2* out = reinterpret_cast<uint2*>(dq + e0);
+      for (int i = threadIdx.x; i < rows * kChunks; i += blockDim.x) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (nacc > 0) {
+          float4 w[kAccWays];
 #pragma unroll
-    for (int m = 0; m < kAccWays; ++m)
-      if (m < nacc) w[m] = acc[i + (long long)m * acc_stride_vec4];
-    float4 v = w[0];
+          for (int m = 0; m < kAccWays; ++m)
+            if (m < nacc) w[m] = a[i + (long long)m * acc_stride_vec4];
+          v = w[0];
 #pragma unroll
-    for (int m = 1; m < kAccWays; ++m) {
-      if (m < nacc) {
-        v.x += w[m].x; v.y += w[m].y; v.z += w[m].z; v.w += w[m].w;
+          for (int m = 1; m < kAccWays; ++m) {
+            if (m < nacc) {
+              v.x += w[m].x; v.y += w[m].y; v.z += w[m].z; v.w += w[m].w;
+            }
+          }
+        }
+        out[i] = make_uint2(pack_bf16x2(scale * v.x, scale * v.y), pack_bf16x2(scale * v.z, scale * v.w));
       }
+    } else {
+      const float4* a = acc + (size_t)T * (kTile * kChunks);
+      for (int u = threadIdx.x; u < kTile * kChunks; u += blockDim.x) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (nacc > 0) {
+          // all loads first (at most kAccWays buffers), then the sum in the
+          // fixed order buffer 0, 1, ...
+          float4 w[kAccWays];
+#pragma unroll
+          for (int m = 0; m < kAccWays; ++m)
+            if (m < nacc) w[m] = a[u + (long long)m * acc_stride_vec4];
+          v = w[0];
+#pragma unroll
+          for (int m = 1; m < kAccWays; ++m) {
+            if (m < nacc) {
+              v.x += w[m].x; v.y += w[m].y; v.z += w[m].z; v.w += w[m].w;
+            }
+          }
+          v.x *= scale; v.y *= scale; v.z *= scale; v.w *= scale;
+        }
+        const int row = u % kTile, ch = u / kTile;
+        *reinterpret_cast<uint2*>(stage + row * kRowBytes + ch * 8) =
+            make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+      }
+      __syncthreads();
+      uint4* out = reinterpret_cast<uint4*>(dq + ((size_t)bh * S + (size_t)j * kTile) * HD);
+      for (int w = threadIdx.x; w < rows * (HD / 8); w += blockDim.x) {
+        const int row = w / (HD / 8), piece = w % (HD / 8);
+        out[w] = *reinterpret_cast<const uint4*>(stage + row * kRowBytes + piece * 16);
+      }
+      __syncthreads();
     }
-    uint2 o;
-    o.x = pack_bf16x2(scale * v.x, scale * v.y);
-    o.y = pack_bf16x2(scale * v.z, scale * v.w);
-    out[i] = o;
   }
 }
 
@@ -228,12 +269,15 @@ cudaError_t launch_status_collect(const uint32_t* slots, int n, void* hdr, cudaS
   return cudaGetLastError();
 }
 
-cudaError_t launch_convert(const float* dqacc, void* dq, long long elems, float scale,
-                           long long acc_stride, int ways, int causal, int N, int S, int d, int grid,
-                           const int* count, cudaStream_t stream) {
-  convert_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dqacc),
-                                           reinterpret_cast<uint2*>(dq), elems / 4, scale,
-                                           acc_stride / 4, ways, causal, N, S, d, count);
+cudaError_t launch_convert(const float* dqacc, void* dq, int ntiles, float scale, long long acc_stride,
+                           int ways, int causal, int N, int S, int d, int grid, const int* count,
+                           cudaStream_t stream) {
+  const float4* a = reinterpret_cast<const float4*>(dqacc);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(dq);
+  if (d == 128)
+    convert_kernel<128><<<grid, 256, 0, stream>>>(a, out, ntiles, scale, acc_stride / 4, ways, causal, N, S, count);
+  else
+    convert_kernel<64><<<grid, 256, 0, stream>>>(a, out, ntiles, scale, acc_stride / 4, ways, causal, N, S, count);
   return cudaGetLastError();
 }
 

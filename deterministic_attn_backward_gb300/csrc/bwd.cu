@@ -10,15 +10,21 @@
 //     dV_i += P^T dO_j                      (P^T read from tensor memory)
 //     dS^T = P^T o (dP^T - D_j)             (softmax warps -> shared memory)
 //     dK_i += dS^T Q_j
-//     dQ_j partial = dS K_i                 (as dQ^T = K_i^T dS^T for d = 128)
+//     dQ_j partial = dS K_i                 (Q rows on tensor-memory lanes)
 // dK_i and dV_i stay in tensor memory for the whole chain (the KV-chain
 // constraint of the DASH DAG model, technical summary section 2.1) and are
 // written once at its end.  The dQ partial is added to an f32 accumulator in
 // global memory by the reducer warps: for the deterministic schedules in the
 // fixed order rank(i, j) (technical summary section 1: a fixed accumulation
-// order for dQ), waiting on per-(head, Q tile, eighth, buffer) semaphores
-// with acquire loads and publishing with a release store; for ATOMIC with
-// unordered float adds.  For the deterministic schedules the same kernel then
+// order for dQ), gated by per-(head, Q tile, eighth, buffer) semaphores; for
+// ATOMIC with unordered float adds.  d = 128: the partial is dQ^T (d on
+// tensor-memory lanes), a reducer thread holds one d index over 64 Q rows and
+// a warp's 32 consecutive d indices form one 128-byte segment of a row of the
+// row-major accumulator [B*H*S][d].  d = 64: the partial is dQ (Q rows on
+// lanes) and the accumulator is stored chunk-major per 128-row tile,
+// [d/4][128 rows][4] f32, so that a thread adds 16 bytes at a time and a
+// warp's 32 rows of a chunk form 512 contiguous bytes.  For the deterministic
+// schedules the same kernel then
 // converts dQ to bf16 in its tail: a CTA without units left converts the dQ
 // tiles whose semaphores show every contribution in.
 //
@@ -26,6 +32,8 @@
 //   warp 0      TMA producer (K_i, V_i per chain; Q_j, dO_j, LSE_j, D_j per
 //               step, double-buffered) and tensor-memory allocation
 //   warp 1      MMA issuer (one thread)
+//   warp 3      dQ publisher (ordered schedules): releases each contribution
+//               once the reducers' adds are in
 //   warps 4-11  softmax / dS, two warpgroups of 64 Q columns each (thread =
 //               KV row), and the chain epilogue (dV by one, dK by the other)
 //   warps 12-19 dQ reducer, one eighth of the dQ tile and one semaphore each
@@ -61,18 +69,22 @@ struct Cfg {
   static constexpr int kOffDD = kOffLse + 1024;            // [2][128] f32
   static constexpr int kOffBar = kOffDD + 1024;
   static constexpr int kOffMisc = kOffBar + 256;
-  static constexpr int kSmemBytes = kOffMisc + 64;
+  static constexpr int kOffPub = kOffMisc + 64;            // [2][8] (semaphore, value) to release
+  static constexpr int kSmemBytes = kOffPub + 2 * 8 * 8;
   // Tensor memory columns (512 allocated).
   static constexpr uint32_t kColDV = 0;
   static constexpr uint32_t kColDK = HD;
   static constexpr uint32_t kColS = 2 * HD;                // S^T, then P^T (bf16, 64 cols)
   static constexpr uint32_t kColDP = 2 * HD + 128;
   static constexpr uint32_t kColDQ = (HD == 128) ? kColDP : 384;  // d=128 reuses dP
+  static constexpr int kChunks = HD / 4;                   // 16-byte chunks of a dQ row
+  // d = 64: chunk-major accumulator tiles [d/4][128][4]; d = 128: row-major.
+  static constexpr bool kChunkMajor = (HD == 64);
   // Instruction descriptors.
   static constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
   static constexpr uint32_t kIdAcc = idesc_bf16(128, HD, 0, 1);  // dV, dK
-  static constexpr uint32_t kIdDQ = (HD == 128) ? idesc_bf16(128, 128, 1, 1)   // dQ^T
-                                                : idesc_bf16(128, 64, 1, 1);   // dQ
+  static constexpr uint32_t kIdDQ = (HD == 128) ? idesc_bf16(128, 128, 1, 1)   // dQ^T = K^T dS^T
+                                                : idesc_bf16(128, 64, 1, 1);   // dQ = dS K
 };
 
 struct Bars {
@@ -83,6 +95,7 @@ struct Bars {
   uint64_t acc_full, acc_empty;
   uint64_t unit_full[2], unit_empty[2];
   uint64_t drain;
+  uint64_t pub_full[2], pub_empty[2]; // reducers -> publisher, publisher -> reducers
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
@@ -167,9 +180,14 @@ static __device__ __noinline__ bool final_wait(const uint32_t* sem, uint32_t tar
 // been claimed by a running CTA before any tile is, and no unit waits for a
 // tile, so these waits always end.  The arithmetic is the convert pass's:
 // the buffers added in index order, times scale, rounded to bf16 (RN-even),
-// so dQ has the same bits whichever of the two wrote it.
+// so dQ has the same bits whichever of the two wrote it.  A chunk-major tile
+// (d = 64) is read 16 bytes per thread (coalesced), the bf16 result goes
+// through shared memory (free once the roles are done) and out row by row.
 template <int HD, bool kRagged>
-__device__ __forceinline__ void tail_convert(const BwdParams& p, Misc* misc, const WaitCtl& wc) {
+__device__ __forceinline__ void tail_convert(const BwdParams& p, Misc* misc, uint8_t* smem,
+                                             const WaitCtl& wc) {
+  constexpr int kChunks = HD / 4;
+  constexpr int kRowBytes = HD * 2 + 16;                 // padded bf16 row in shared memory
   const int tid = threadIdx.x;
   const int ntiles = p.BH * p.N;
   const size_t stride4 = (size_t)p.acc_stride / 4;
@@ -196,39 +214,73 @@ __device__ __forceinline__ void tail_convert(const BwdParams& p, Misc* misc, con
     fence_acq_rel_gpu();
     // rows of the tile inside the head (a partial last tile stops at S)
     const int rows = kRagged ? min(kTile, p.S - j * kTile) : kTile;
-    const size_t e0 = ((size_t)bh * p.S + (size_t)j * kTile) * HD;
-    const float4* acc = reinterpret_cast<const float4*>(p.dqacc + e0);
-    uint2* out = reinterpret_cast<uint2*>(p.dq + e0);
-    const int n4 = rows * (HD / 4);
-    if (nacc == 0) {
-      for (int i = tid; i < n4; i += kThreads) out[i] = make_uint2(0u, 0u);
-    } else {
-      // two vectors per thread and pass: all loads first, then the sums
-      for (int i0 = tid; i0 < n4; i0 += 2 * kThreads) {
-        float4 w[2][kAccWays];
+    if constexpr (HD == 128) {
+      // row-major accumulator: 16-byte vectors, two per thread and pass, all
+      // loads first, then the sums
+      const size_t e0 = ((size_t)bh * p.S + (size_t)j * kTile) * HD;
+      const float4* acc = reinterpret_cast<const float4*>(p.dqacc + e0);
+      uint2* out = reinterpret_cast<uint2*>(p.dq + e0);
+      const int n4 = rows * (HD / 4);
+      if (nacc == 0) {
+        for (int i = tid; i < n4; i += kThreads) out[i] = make_uint2(0u, 0u);
+      } else {
+        for (int i0 = tid; i0 < n4; i0 += 2 * kThreads) {
+          float4 w[2][kAccWays];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int m = 0; m < kAccWays; ++m)
+              if (m < nacc && i0 + h * kThreads < n4) w[h][m] = __ldcg(acc + i0 + h * kThreads + m * stride4);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int i = i0 + h * kThreads;
+            if (i >= n4) break;
+            float4 v = w[h][0];
+#pragma unroll
+            for (int m = 1; m < kAccWays; ++m) {
+              if (m < nacc) {
+                v.x += w[h][m].x; v.y += w[h][m].y; v.z += w[h][m].z; v.w += w[h][m].w;
+              }
+            }
+            out[i] = make_uint2(pack_bf16x2(p.scale * v.x, p.scale * v.y),
+                                pack_bf16x2(p.scale * v.z, p.scale * v.w));
+          }
+        }
+      }
+    } else {
+      // chunk-major tile: chunk units u = chunk * 128 + row, consecutive
+      // threads on consecutive rows (coalesced 16-byte loads); the bf16
+      // result is staged in shared memory (free once the roles are done)
+      // and written row by row
+      const float4* acc = reinterpret_cast<const float4*>(p.dqacc) + ((size_t)bh * p.N + j) * (kTile * kChunks);
+      for (int u = tid; u < kTile * kChunks; u += kThreads) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (nacc > 0) {
+          float4 w[kAccWays];
 #pragma unroll
           for (int m = 0; m < kAccWays; ++m)
-            if (m < nacc && i0 + h * kThreads < n4)
-              w[h][m] = __ldcg(acc + i0 + h * kThreads + m * stride4);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int i = i0 + h * kThreads;
-          if (i >= n4) break;
-          float4 v = w[h][0];
+            if (m < nacc) w[m] = __ldcg(acc + u + m * stride4);
+          v = w[0];
 #pragma unroll
           for (int m = 1; m < kAccWays; ++m) {
             if (m < nacc) {
-              v.x += w[h][m].x; v.y += w[h][m].y; v.z += w[h][m].z; v.w += w[h][m].w;
+              v.x += w[m].x; v.y += w[m].y; v.z += w[m].z; v.w += w[m].w;
             }
           }
-          out[i] = make_uint2(pack_bf16x2(p.scale * v.x, p.scale * v.y),
-                              pack_bf16x2(p.scale * v.z, p.scale * v.w));
+          v.x *= p.scale; v.y *= p.scale; v.z *= p.scale; v.w *= p.scale;
         }
+        const int row = u % kTile, ch = u / kTile;
+        *reinterpret_cast<uint2*>(smem + row * kRowBytes + ch * 8) =
+            make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+      }
+      __syncthreads();
+      uint4* out = reinterpret_cast<uint4*>(p.dq + ((size_t)bh * p.S + (size_t)j * kTile) * HD);
+      for (int w = tid; w < rows * (HD / 8); w += kThreads) {
+        const int row = w / (HD / 8), piece = w % (HD / 8);
+        out[w] = *reinterpret_cast<const uint4*>(smem + row * kRowBytes + piece * 16);
       }
     }
-    __syncthreads();  // misc->conv is rewritten for the next tile
+    __syncthreads();  // misc->conv and the staging rows are rewritten for the next tile
   }
 }
 
@@ -260,7 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1 + 8);
       mbar_init(&bars->unit_full[s], 1);
-      mbar_init(&bars->unit_empty[s], 1 + 8 + 8);
+      mbar_init(&bars->unit_empty[s], 1 + 8 + 8 + 1);
+      mbar_init(&bars->pub_full[s], 8 * 32);
+      mbar_init(&bars->pub_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
@@ -477,6 +531,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       drain_wait(&bars->drain, 0, p.hdr, p.timeout_ns, 3);
     }
     __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------ dQ publisher
+    // Ordered schedules only (ATOMIC has no semaphores: this warp just
+    // follows the units).  Every reducer thread arrives (release, CTA scope)
+    // on pub_full after its adds of a step; this warp acquires that phase
+    // and then, per eighth (lane k: eighth k), fences at gpu scope and stores
+    // rank + 1.  A release is cumulative: the adds ordered before the arrive
+    // that the acquire observed are ordered before the semaphore store for
+    // whoever acquires it.  So the reducer warps do not wait for their adds
+    // to be performed before draining and adding the next partial.
+    const uint2* slots = reinterpret_cast<const uint2*>(smem + C::kOffPub);
+    int s = 0, uidx = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = uidx & 1;
+      if (!warp_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 51)) break;
+      const int U = misc->ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->unit_empty[slot]);
+      ++uidx;
+      if (U < 0) break;
+      const int steps = k_unit_steps(p, U % p.units_per_head);
+      for (int t = 0; t < steps; ++t) {
+        if (deterministic) {
+          if (!warp_wait(&bars->pub_full[s & 1], (s >> 1) & 1, wc, 53)) { ok = false; break; }
+          if (lane < kSubTiles) {
+            const uint2 e = slots[(s & 1) * kSubTiles + lane];
+            fence_acq_rel_gpu();
+            st_release_gpu(p.sem + e.x, e.y);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->pub_empty[s & 1]);
+        }
+        ++s;
+      }
+    }
   } else if (warp >= kSoftmaxWarp0 && warp < kReducerWarp0) {
     // ------------------------------------------------------ softmax / dS
     // Two warpgroups; warpgroup h owns Q columns 64h .. 64h+63 of the tile.
@@ -634,25 +724,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     // tensor-memory quadrant of the dQ partial into registers at once (so
     // the tensor memory is free for the next partial), then adds that
     // eighth of the tile into the f32 accumulator:
-    //   d = 128 (dQ^T, lanes = d):  d columns 32*quad.., Q rows 64*half..+63
-    //   d =  64 (dQ, lanes = Q rows): Q rows 32*quad.., d columns 32*half..+31
+    //   d = 128 (dQ^T, lanes = d): d index 32*quad + lane, Q rows
+    //     64*half .. + 63; each add is one float, a warp's 32 adds of a row
+    //     are 128 contiguous bytes of the row-major accumulator;
+    //   d = 64 (dQ, lanes = Q rows): Q row 32*quad + lane, d columns
+    //     32*half .. + 31; each add is 16 bytes into the chunk-major tile
+    //     [d/4][128][4], a warp's 32 rows of a chunk are 512 contiguous bytes.
     // For the ordered schedules every eighth of every accumulation buffer has
     // its own semaphore, so consecutive contributors to one dQ tile overlap
     // on different eighths and buffers while each element of a buffer still
-    // receives its partial sums in rank order.
+    // receives its partial sums in rank order.  A buffer's first contribution
+    // stores.  The release after the adds is the publisher's (warp 3).
     const int quad = warp & 3;                          // tensor-memory lane quadrant
     const int half = (warp - kReducerWarp0) >> 2;
     const int sub = half * 4 + quad;                    // sub-tile / semaphore index
     const int r = quad * 32 + lane;                     // d index (d = 128) or Q row (d = 64)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     constexpr int kVals = (HD == 128) ? 64 : 32;        // values per thread per step
-    // Inside a unit, a step's contribution is published (fence, then release
-    // of the semaphore) only after the next step's partial has been drained:
-    // the fence waits for the adds to complete, and draining first frees the
-    // tensor memory for the next dP without waiting for that.  The last step
-    // of a unit publishes at once.
-    uint32_t* pend_sem = nullptr;
-    uint32_t pend_val = 0;
+    uint2* slots = reinterpret_cast<uint2*>(smem + C::kOffPub);
     int s = 0, uidx = 0;
     bool ok = true;
     while (ok) {
@@ -672,19 +761,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         const int rank = deterministic ? k_rank(p, st.kv, st.q) : 0;
         const int way = rank % p.acc_ways, lrank = rank / p.acc_ways;
         const size_t sem_idx = (((size_t)bh * p.N + st.q) * kSubTiles + sub) * p.acc_ways + way;
-        uint32_t* sem = p.sem + sem_idx;
-        const uint32_t sem_detail = (uint32_t)sem_idx;
         const bool store = deterministic && lrank == 0;  // a buffer's first contribution overwrites
-        const size_t row0 = (size_t)bh * p.S + (size_t)st.q * kTile;
         float* acc = p.dqacc + (size_t)way * (size_t)p.acc_stride;
-        float* base = (HD == 128) ? acc + (row0 + (size_t)half * 64) * HD + r
-                                  : acc + (row0 + (size_t)r) * HD + half * 32;
-        // Rows past the end of a partial last Q tile belong to the next head
-        // in the accumulator: never touched (their partial sums are zero).
-        const int row_lim = p.S - st.q * kTile - ((HD == 128) ? half * 64 : r);
-        const int nvalid = !kRagged ? ((HD == 128) ? 64 : 1)
-                           : (HD == 128) ? (row_lim < 0 ? 0 : (row_lim > 64 ? 64 : row_lim))
-                                         : (row_lim > 0 ? 1 : 0);
+        // d = 128: row-major, this thread's column of Q rows 64*half ..;
+        // d = 64: chunk-major, this thread's row in its first chunk
+        const size_t row0 = (size_t)bh * p.S + (size_t)st.q * kTile;
+        float* base = C::kChunkMajor
+                          ? acc + (((size_t)(bh * p.N + st.q) * C::kChunks + (size_t)half * (C::kChunks / 2)) * kTile + r) * 4
+                          : acc + (row0 + (size_t)half * 64) * HD + r;
+        // d = 128: rows past the end of a partial last Q tile belong to the
+        // next head in the row-major accumulator and are never touched (their
+        // partial sums are zero).  d = 64: they lie in the tile's padding.
+        const int row_lim = p.S - st.q * kTile - half * 64;
+        const int nvalid = (!kRagged || C::kChunkMajor) ? 64 : (row_lim < 0 ? 0 : (row_lim > 64 ? 64 : row_lim));
         if (!warp_wait(&bars->dq_full, s & 1, wc, 41)) { ok = false; break; }
         tc_fence_after();
         uint32_t v[kVals];
@@ -695,32 +784,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->dq_empty);
-        if (pend_sem != nullptr) {  // publish the previous step's contribution
-          fence_acq_rel_gpu();
-          __syncwarp();
-          if (lane == 0) st_release_gpu(pend_sem, pend_val);
-          pend_sem = nullptr;
-        }
         if (deterministic) {
           int g = 1;
-          if (lane == 0) g = sem_wait(sem, (uint32_t)lrank, wc, sem_detail) ? 1 : 0;
+          if (lane == 0) g = sem_wait(p.sem + sem_idx, (uint32_t)lrank, wc, (uint32_t)sem_idx) ? 1 : 0;
           g = __shfl_sync(0xffffffffu, g, 0);
           if (!g) { ok = false; break; }
+          if (p.plain_add && !store) fence_acq_rel_gpu();
         }
         if (HD == 128) {
           if (store) {
-            if (nvalid == 64) {
 #pragma unroll
-              for (int q = 0; q < 64; ++q) base[(size_t)q * HD] = __uint_as_float(v[q]);
-            } else {
-#pragma unroll
-              for (int q = 0; q < 64; ++q)
-                if (q < nvalid) base[(size_t)q * HD] = __uint_as_float(v[q]);
-            }
+            for (int q = 0; q < 64; ++q)
+              if (q < nvalid) base[(size_t)q * HD] = __uint_as_float(v[q]);
           } else if (deterministic && p.plain_add) {
             // load + add + store, the same IEEE adds in the same order as
             // the red (only this contributor touches the sub-tile now)
-            fence_acq_rel_gpu();
 #pragma unroll
             for (int c = 0; c < 64; c += 16) {
               float a[16];
@@ -732,50 +810,40 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
                 if (c + k < nvalid) base[(size_t)(c + k) * HD] = a[k] + __uint_as_float(v[c + k]);
             }
           } else {
-            if (nvalid == 64) {
 #pragma unroll
-              for (int q = 0; q < 64; ++q) {
-                red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
-                // Ordered schedules: spread the adds out so that they do not
-                // fill the SM's memory-instruction queue in one burst (the
-                // softmax warps' shared-memory loads wait behind them).
-                if (deterministic && (q & 7) == 7) __nanosleep(20);
-              }
-            } else {  // the last, partial Q tile
-#pragma unroll
-              for (int q = 0; q < 64; ++q)
-                if (q < nvalid) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
+            for (int q = 0; q < 64; ++q) {
+              if (q < nvalid) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
+              // Ordered schedules: spread the adds out so that they do not
+              // fill the SM's memory-instruction queue in one burst (the
+              // softmax warps' shared-memory loads wait behind them).
+              if (deterministic && (q & 7) == 7) __nanosleep(20);
             }
           }
         } else {
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            if (nvalid == 0) break;                  // this Q row lies past S
+          for (int m = 0; m < kVals / 4; ++m) {
+            float* dst = base + (size_t)m * (kTile * 4);
             const float a0 = __uint_as_float(v[4 * m]), a1 = __uint_as_float(v[4 * m + 1]);
             const float a2 = __uint_as_float(v[4 * m + 2]), a3 = __uint_as_float(v[4 * m + 3]);
             if (store) {
-              reinterpret_cast<float4*>(base)[m] = make_float4(a0, a1, a2, a3);
+              *reinterpret_cast<float4*>(dst) = make_float4(a0, a1, a2, a3);
             } else if (deterministic && p.plain_add) {
-              if (m == 0) fence_acq_rel_gpu();
-              const float4 b = ld_cg_v4_f32(base + 4 * m);
-              reinterpret_cast<float4*>(base)[m] = make_float4(b.x + a0, b.y + a1, b.z + a2, b.w + a3);
+              // load + add + store: the same IEEE adds in the same order
+              const float4 b = ld_cg_v4_f32(dst);
+              *reinterpret_cast<float4*>(dst) = make_float4(b.x + a0, b.y + a1, b.z + a2, b.w + a3);
             } else {
-              red_add_v4_f32(base + 4 * m, a0, a1, a2, a3);
+              red_add_v4_f32(dst, a0, a1, a2, a3);
             }
           }
         }
         if (deterministic) {
-          // Publish: the warp's writes are ordered before the release of
-          // rank + 1 (fence per lane, warp barrier, lane 0's release store).
-          // (rank + 1 is released after the next step's drain, see above)
-          if (t + 1 < steps) {
-            pend_sem = sem;
-            pend_val = (uint32_t)lrank + 1u;
-          } else {
-            fence_acq_rel_gpu();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(sem, (uint32_t)lrank + 1u);
-          }
+          // Hand the release of rank + 1 to the publisher: every thread
+          // arrives (release, CTA scope) after its adds.  The slot of this
+          // parity is free once the publisher has released step s - 2.
+          if (s >= 2 && !warp_wait(&bars->pub_empty[s & 1], ((s >> 1) - 1) & 1, wc, 44)) { ok = false; break; }
+          if (lane == 0) slots[(s & 1) * kSubTiles + sub] = make_uint2((uint32_t)sem_idx, (uint32_t)lrank + 1u);
+          __syncwarp();
+          mbar_arrive(&bars->pub_full[s & 1]);
         }
         ++s;
       }
@@ -788,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
-  if (p.fuse_convert) tail_convert<HD, kRagged>(p, misc, wc);
+  if (p.fuse_convert) tail_convert<HD, kRagged>(p, misc, smem, wc);
 }
 
 }  // namespace

@@ -292,6 +292,17 @@ __device__ __forceinline__ float4 ld_cg_v4_f32(const float* p) {
   return v;
 }
 
+// Relaxed (gpu scope) 16-byte load: values other SMs have published, read
+// after an acquire chain has ordered them before this thread.
+__device__ __forceinline__ float4 ld_relaxed_v4_f32(const float* p) {
+  float4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
