@@ -31,7 +31,8 @@
 // Warp roles (20 warps):
 //   warp 0      TMA producer (K_i, V_i per chain; Q_j, dO_j, LSE_j, D_j per
 //               step, double-buffered) and tensor-memory allocation
-//   warp 1      MMA issuer (one thread)
+//   warp 1      MMA issuer of S^T and dP^T (one thread)
+//   warp 2      MMA issuer of dV, the dQ partial and dK (one thread)
 //   warp 3      dQ publisher (ordered schedules): releases each contribution
 //               once the reducers' adds are in
 //   warps 4-11  softmax / dS, two warpgroups of 64 Q columns each (thread =
@@ -94,7 +95,7 @@ struct Bars {
   uint64_t dv_done, ds_free, dq_full, dq_empty;
   uint64_t acc_full, acc_empty;
   uint64_t unit_full[2], unit_empty[2];
-  uint64_t drain;
+  uint64_t drain, drain2;
   uint64_t pub_full[2], pub_empty[2]; // reducers -> publisher, publisher -> reducers
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
@@ -307,12 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
-    mbar_init(&bars->kv_empty, 1);
+    mbar_init(&bars->kv_empty, 2);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->q_full[s], 1);
-      mbar_init(&bars->q_empty[s], 1 + 8);
+      mbar_init(&bars->q_empty[s], 2 + 8);
       mbar_init(&bars->unit_full[s], 1);
-      mbar_init(&bars->unit_empty[s], 1 + 8 + 8 + 1);
+      mbar_init(&bars->unit_empty[s], 2 + 8 + 8 + 1);
       mbar_init(&bars->pub_full[s], 8 * 32);
       mbar_init(&bars->pub_empty[s], 1);
     }
@@ -327,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain2, 1);
     misc->abort = 0;
     fence_mbar_init();
   }
@@ -407,17 +409,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         if (issued[st] > 0) drain_wait(&bars->q_full[st], (issued[st] - 1) & 1, p.hdr, p.timeout_ns, 2);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Per step s (tile i, j): dV(s), dQ(s), then S(s+1) of the next step of
-    // the same chain, dK(s), dP(s+1).  S(s+1) and dP(s+1) thus run while the
-    // softmax warps still work on step s, dK(s) hides the reducer's drain of
-    // dQ(s), and the tensor pipe always has work queued.  At a chain boundary
-    // S and dP of the new chain's first step are issued once its K/V landed.
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing threads on two SM sub-partitions.  With one thread, S^T of
+    // the next step queued behind that thread's wait for dS of the current
+    // step; split, each chain of products is issued as soon as its own
+    // inputs are ready:
+    //   warp 1, the "forward" products of every step: S^T = K Q^T once dV of
+    //     the previous step has read P from the S columns, then dP^T = V dO^T
+    //     once its columns are free (d = 128: the reducers have drained the
+    //     previous dQ partial, which shares them; d = 64: the softmax has
+    //     read the previous dP);
+    //   warp 2, the "backward" products: dV += P^T dO once the softmax has
+    //     written P, then the dQ partial (d = 128: dQ^T = K^T dS^T; d = 64:
+    //     dQ = dS K) and dK += dS^T Q once it has written dS.
+    // A commit tracks only the MMAs of the thread that issues it, so the
+    // barriers that release a Q/dO stage and the K/V tiles take one commit
+    // from each issuer.
     if (lane == 0) {
+      const bool fwd = (warp == 1);
       // Descriptors of every operand at K step 0, built once; step k adds a
-      // compile-time offset, so issuing an MMA costs almost no instructions
-      // (this thread shares its sub-partition with busy warps).
+      // compile-time offset.
       const uint64_t dK_k = desc_kmajor(sbase + C::kOffK, 0, 128);
       const uint64_t dK_mn = desc_mnmajor(sbase + C::kOffK, 0, 128);
       const uint64_t dV_k = desc_kmajor(sbase + C::kOffV, 0, 128);
@@ -431,25 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       constexpr uint64_t kStageOff = C::kTileBytes >> 4;
       const uint32_t tS = tbase + C::kColS, tDP = tbase + C::kColDP, tDV = tbase + C::kColDV;
       const uint32_t tDK = tbase + C::kColDK, tDQ = tbase + C::kColDQ;
-      auto issue_s = [&](int stage) {
-        const uint64_t q0 = dQ_k0 + (uint64_t)stage * kStageOff;
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tS, dK_k + koff_kmajor(k, 128), q0 + koff_kmajor(k, 128), C::kIdS, k > 0);
-        mma_commit(&bars->s_full);
-      };
-      auto issue_dp = [&](int stage) {
-        const uint64_t o0 = dDO_k0 + (uint64_t)stage * kStageOff;
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tDP, dV_k + koff_kmajor(k, 128), o0 + koff_kmajor(k, 128), C::kIdS, k > 0);
-        mma_commit(&bars->dp_full);
-      };
       int s = 0, chain = 0, uidx = 0;
-      bool ok = true, pre = false;
+      bool ok = true;
       while (ok) {
         const int slot = uidx & 1;
-        if (!mbar_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, 10)) break;
+        if (!mbar_wait(&bars->unit_full[slot], (uidx >> 1) & 1, wc, fwd ? 10 : 22)) break;
         const int U = misc->ring[slot];
         mbar_arrive(&bars->unit_empty[slot]);
         ++uidx;
@@ -459,76 +457,84 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         for (int t = 0; t < steps; ++t) {
           const Step st = k_step(p, u, t, steps);
           const int stage = s & 1;
-          if (!pre) {
+          if (fwd) {
             if (st.chain_first && !mbar_wait(&bars->kv_full, chain & 1, wc, 11)) { ok = false; break; }
             if (!mbar_wait(&bars->q_full[stage], (s >> 1) & 1, wc, 12)) { ok = false; break; }
             if (s > 0 && !mbar_wait(&bars->dv_done, (s - 1) & 1, wc, 13)) { ok = false; break; }
             tc_fence_after();
-            issue_s(stage);
-            if (HD == 128 && s > 0 && !mbar_wait(&bars->dq_empty, (s - 1) & 1, wc, 14)) { ok = false; break; }
-            tc_fence_after();
-            issue_dp(stage);
-          }
-          // dV += P^T dO; P^T from tensor memory, its two 64-column halves
-          // packed at the start of each half of the S columns
-          if (!mbar_wait(&bars->p_full, s & 1, wc, 15)) { ok = false; break; }
-          if (st.chain_first && chain > 0 && !mbar_wait(&bars->acc_empty, (chain - 1) & 1, wc, 16)) { ok = false; break; }
-          tc_fence_after();
-          {
-            const uint64_t o0 = dDO_mn0 + (uint64_t)stage * kStageOff;
-            const uint32_t acc0 = st.chain_first ? 0u : 1u;
+            {
+              const uint64_t q0 = dQ_k0 + (uint64_t)stage * kStageOff;
 #pragma unroll
-            for (int k = 0; k < kTile / 16; ++k)
-              mma_ts(tDV, tS + (k >> 2) * 64 + (k & 3) * 8, o0 + koff_mnmajor(k), C::kIdAcc,
-                     k == 0 ? acc0 : 1u);
-          }
-          mma_commit(&bars->dv_done);
-          // dQ partial (d = 128: dQ^T = K^T dS^T; d = 64: dQ = dS K)
-          if (!mbar_wait(&bars->ds_full, s & 1, wc, 17)) { ok = false; break; }
-          if (HD == 64 && s > 0 && !mbar_wait(&bars->dq_empty, (s - 1) & 1, wc, 18)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < kTile / 16; ++k) {
-            const uint64_t a = ((HD == 128) ? dK_mn : dDS_mn) + koff_mnmajor(k);
-            const uint64_t b = ((HD == 128) ? dDS_mn : dK_mn) + koff_mnmajor(k);
-            mma_ss(tDQ, a, b, C::kIdDQ, k > 0);
-          }
-          mma_commit(&bars->dq_full);
-          const bool next = !st.chain_last;  // the next step continues this chain
-          if (next) {
-            const int st1 = (s + 1) & 1;
-            if (!mbar_wait(&bars->q_full[st1], ((s + 1) >> 1) & 1, wc, 19)) { ok = false; break; }
-            if (!mbar_wait(&bars->dv_done, s & 1, wc, 20)) { ok = false; break; }  // P^T(s) consumed
+              for (int k = 0; k < HD / 16; ++k)
+                mma_ss(tS, dK_k + koff_kmajor(k, 128), q0 + koff_kmajor(k, 128), C::kIdS, k > 0);
+              mma_commit(&bars->s_full);
+            }
+            if (s > 0 && !mbar_wait(HD == 128 ? &bars->dq_empty : &bars->ds_full, (s - 1) & 1, wc, 14)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
-            issue_s(st1);
-          }
-          // dK += dS^T Q
-          {
-            const uint64_t q0 = dQ_mn0 + (uint64_t)stage * kStageOff;
-            const uint32_t acc0 = st.chain_first ? 0u : 1u;
+            {
+              const uint64_t o0 = dDO_k0 + (uint64_t)stage * kStageOff;
 #pragma unroll
-            for (int k = 0; k < kTile / 16; ++k)
-              mma_ss(tDK, dDS_k + koff_kmajor(k, 128), q0 + koff_mnmajor(k), C::kIdAcc, k == 0 ? acc0 : 1u);
-          }
-          mma_commit(&bars->q_empty[stage]);
-          mma_commit(&bars->ds_free);
-          if (st.chain_last) {
-            mma_commit(&bars->acc_full);
-            mma_commit(&bars->kv_empty);
-            ++chain;
-          }
-          if (next) {
-            if (HD == 128 && !mbar_wait(&bars->dq_empty, s & 1, wc, 21)) { ok = false; break; }
+              for (int k = 0; k < HD / 16; ++k)
+                mma_ss(tDP, dV_k + koff_kmajor(k, 128), o0 + koff_kmajor(k, 128), C::kIdS, k > 0);
+              mma_commit(&bars->dp_full);
+            }
+            mma_commit(&bars->q_empty[stage]);
+            if (st.chain_last) {
+              mma_commit(&bars->kv_empty);
+              ++chain;
+            }
+          } else {
+            // dV += P^T dO; P^T from tensor memory, its two 64-column halves
+            // packed at the start of each half of the S columns
+            if (!mbar_wait(&bars->p_full, s & 1, wc, 15)) { ok = false; break; }
+            if (st.chain_first && chain > 0 && !mbar_wait(&bars->acc_empty, (chain - 1) & 1, wc, 16)) { ok = false; break; }
             tc_fence_after();
-            issue_dp((s + 1) & 1);
+            {
+              const uint64_t o0 = dDO_mn0 + (uint64_t)stage * kStageOff;
+              const uint32_t acc0 = st.chain_first ? 0u : 1u;
+#pragma unroll
+              for (int k = 0; k < kTile / 16; ++k)
+                mma_ts(tDV, tS + (k >> 2) * 64 + (k & 3) * 8, o0 + koff_mnmajor(k), C::kIdAcc,
+                       k == 0 ? acc0 : 1u);
+            }
+            mma_commit(&bars->dv_done);
+            // dQ partial (d = 128: dQ^T = K^T dS^T; d = 64: dQ = dS K)
+            if (!mbar_wait(&bars->ds_full, s & 1, wc, 17)) { ok = false; break; }
+            if (HD == 64 && s > 0 && !mbar_wait(&bars->dq_empty, (s - 1) & 1, wc, 18)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kTile / 16; ++k) {
+              const uint64_t a = ((HD == 128) ? dK_mn : dDS_mn) + koff_mnmajor(k);
+              const uint64_t b = ((HD == 128) ? dDS_mn : dK_mn) + koff_mnmajor(k);
+              mma_ss(tDQ, a, b, C::kIdDQ, k > 0);
+            }
+            mma_commit(&bars->dq_full);
+            // dK += dS^T Q
+            {
+              const uint64_t q0 = dQ_mn0 + (uint64_t)stage * kStageOff;
+              const uint32_t acc0 = st.chain_first ? 0u : 1u;
+#pragma unroll
+              for (int k = 0; k < kTile / 16; ++k)
+                mma_ss(tDK, dDS_k + koff_kmajor(k, 128), q0 + koff_mnmajor(k), C::kIdAcc, k == 0 ? acc0 : 1u);
+            }
+            mma_commit(&bars->q_empty[stage]);
+            mma_commit(&bars->ds_free);
+            if (st.chain_last) {
+              mma_commit(&bars->acc_full);
+              mma_commit(&bars->kv_empty);
+              ++chain;
+            }
           }
-          pre = next;
           ++s;
         }
       }
-      // Teardown: wait until every issued MMA has completed.
-      mma_commit(&bars->drain);
-      drain_wait(&bars->drain, 0, p.hdr, p.timeout_ns, 3);
+      // Teardown: wait until every MMA this thread issued has completed.
+      uint64_t* dr = fwd ? &bars->drain : &bars->drain2;
+      mma_commit(dr);
+      drain_wait(dr, 0, p.hdr, p.timeout_ns, fwd ? 3 : 4);
     }
     __syncwarp();
   } else if (warp == 3) {
