@@ -37,9 +37,11 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b) {
 }
 
 // One row of HD bf16 is HD/8 vectors; a warp covers 32 / (HD/8) rows at once.
-// D and LSE2 are laid out per head with S_pad = 128 * ceil(S / 128) rows; the
-// rows past S of a partial last tile get D = 0 and LSE2 = +infinity, so that
-// every P the main kernel forms for them is exactly 0.
+// D and LSE2 = -LSE * log2(e) are laid out per head with S_pad = 128 *
+// ceil(S / 128) rows; the rows past S of a partial last tile get D = 0 and
+// LSE2 = -infinity, so that every P the main kernel forms for them is exactly
+// 0.  (Negated, so that the main kernel forms scale*log2(e) * s + LSE2 with
+// one packed fma per pair of columns.)
 template <int HD>
 __global__ void __launch_bounds__(256) preprocess_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
@@ -67,7 +69,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
     for (long long i = gtid; i < npad; i += nthreads) {
       const long long idx = (i / (S_pad - S)) * S_pad + S + i % (S_pad - S);
       D[idx] = 0.f;
-      lse2[idx] = INFINITY;
+      lse2[idx] = -INFINITY;
     }
   }
   if (dqacc != nullptr) {
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
         const int ir = (int)row;
         const int idx = (S_pad == S) ? ir : (ir / S) * S_pad + ir % S;
         D[idx] = acc;
-        lse2[idx] = lse[row] * kLog2e;
+        lse2[idx] = -(lse[row] * kLog2e);
       }
     }
   }

@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
   Misc* misc = reinterpret_cast<Misc*>(smem + C::kOffMisc);
-  float* s_lse = reinterpret_cast<float*>(smem + C::kOffLse);
+  float* s_lse = reinterpret_cast<float*>(smem + C::kOffLse);  // -LSE*log2(e) of the stage's Q rows
   float* s_dd = reinterpret_cast<float*>(smem + C::kOffDD);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             tma_load_2d(sq + db * C::kBlockBytes, &p.tm_q, &bars->q_full[stage], db * 64, row);
             tma_load_2d(sdo + db * C::kBlockBytes, &p.tm_do, &bars->q_full[stage], db * 64, row);
           }
-          // LSE2 and D are padded to whole tiles per head (+inf / 0 past S)
+          // -LSE*log2(e) and D are padded to whole tiles per head (-inf / 0 past S)
           const size_t prow = (size_t)bh * (p.N * kTile) + (size_t)st.q * kTile;
           bulk_load(s_lse + stage * 128, p.lse2 + prow, 512, &bars->q_full[stage]);
           bulk_load(s_dd + stage * 128, p.D + prow, 512, &bars->q_full[stage]);
@@ -617,8 +617,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         if (!warp_wait(&bars->s_full, s & 1, wc, 32)) { ok = false; break; }
         tc_fence_after();
         // P^T = exp2(S^T * scale*log2(e) - LSE*log2(e)), bf16 pairs written
-        // over the columns this warpgroup has just read.
+        // over the columns this warpgroup has just read.  The stored values
+        // are -LSE*log2(e), so each pair of columns is one packed fma.
         uint32_t pk[32];
+        const unsigned long long c2 = f32x2_pack(p.scale_log2e, p.scale_log2e);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
@@ -628,10 +630,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           for (int e = 0; e < 32; e += 4) {
             const int col = 32 * c + e;          // column within this half
             const float4 l4 = *reinterpret_cast<const float4*>(lse + col);
-            float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2e, -l4.x));
-            float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2e, -l4.y));
-            float p2 = ex2_approx(fmaf(__uint_as_float(v[e + 2]), p.scale_log2e, -l4.z));
-            float p3 = ex2_approx(fmaf(__uint_as_float(v[e + 3]), p.scale_log2e, -l4.w));
+            float x0, x1, x2, x3;
+            f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), c2,
+                                   f32x2_pack(l4.x, l4.y)), x0, x1);
+            f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), c2,
+                                   f32x2_pack(l4.z, l4.w)), x2, x3);
+            float p0 = ex2_approx(x0);
+            float p1 = ex2_approx(x1);
+            float p2 = ex2_approx(x2);
+            float p3 = ex2_approx(x3);
             if (diag) {
               const int qc = 64 * h + col;       // Q column within the tile
               if (r > qc) p0 = 0.f;
@@ -671,10 +678,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             const int col = 16 * c + e;
             const float4 d4 = *reinterpret_cast<const float4*>(dd + col);
             const uint32_t pa = pk[8 * c + (e >> 1)], pb = pk[8 * c + (e >> 1) + 1];
-            const float ds0 = __uint_as_float(pa << 16) * (__uint_as_float(v[e]) - d4.x);
-            const float ds1 = __uint_as_float(pa & 0xFFFF0000u) * (__uint_as_float(v[e + 1]) - d4.y);
-            const float ds2 = __uint_as_float(pb << 16) * (__uint_as_float(v[e + 2]) - d4.z);
-            const float ds3 = __uint_as_float(pb & 0xFFFF0000u) * (__uint_as_float(v[e + 3]) - d4.w);
+            float ds0, ds1, ds2, ds3;
+            f32x2_unpack(mul_f32x2(f32x2_pack(__uint_as_float(pa << 16), __uint_as_float(pa & 0xFFFF0000u)),
+                                   sub_f32x2(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                             f32x2_pack(d4.x, d4.y))), ds0, ds1);
+            f32x2_unpack(mul_f32x2(f32x2_pack(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)),
+                                   sub_f32x2(f32x2_pack(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])),
+                                             f32x2_pack(d4.z, d4.w))), ds2, ds3);
             w8[e >> 1] = pack_bf16x2(ds0, ds1);
             w8[(e >> 1) + 1] = pack_bf16x2(ds2, ds3);
           }

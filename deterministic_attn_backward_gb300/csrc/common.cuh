@@ -43,9 +43,9 @@ constexpr int kSubTiles = 8;  // semaphores (and reducer warps) per dQ tile per 
 
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [B*H*S, d] bf16, box 64 x 128, 128B swizzle
-  const float* lse2;                    // [B*H*S] LSE * log2(e)
-  const float* D;                       // [B*H*S]
-  float* dqacc;                         // [acc_ways][B*H*S, d] f32
+  const float* lse2;                    // [B*H*S_pad] -LSE * log2(e)
+  const float* D;                       // [B*H*S_pad]
+  float* dqacc;                         // [acc_ways][B*H*S_pad*d] f32 (see bwd.cu)
   long long acc_stride;                 // floats between two accumulation buffers
   int acc_ways;                         // kAccWays (ordered schedules) or 1 (atomic)
   __nv_bfloat16* dk;                    // [B*H*S, d]

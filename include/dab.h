@@ -113,7 +113,7 @@ dab_status_t dab_attn_fwd(const void* q, const void* k, const void* v,
 /* Bytes of device workspace that dab_attn_bwd needs for this problem (0 on
  * invalid arguments).  The workspace holds the status word, the dispatch
  * counters, the semaphores (per 128-row dQ tile: one per eighth of the tile
- * and per accumulation buffer), D and LSE*log2(e) per row, and the float32
+ * and per accumulation buffer), D and -LSE*log2(e) per row, and the float32
  * dQ accumulation buffers [ways][B][H][S][d] (four interleaved buffers for
  * the ordered schedules, one for ATOMIC).  It needs no initialisation: the
  * first kernel of every backward call resets what must start at zero.      */
@@ -123,7 +123,7 @@ size_t dab_bwd_workspace_size(int B, int H, int S, int d,
 /* Attention backward.  Inputs Q, K, V, O, dO (bf16) and LSE (f32) as produced
  * by dab_attn_fwd; outputs dQ, dK, dV (bf16), each written in full.
  * Launches, on `stream`:
- *   1. the preprocess kernel: D_r = sum_k dO_rk O_rk (f32), LSE*log2(e),
+ *   1. the preprocess kernel: D_r = sum_k dO_rk O_rk (f32), -LSE*log2(e),
  *      reset of the semaphores, status word and dispatch counter (and, for
  *      ATOMIC, zeroing of the dQ accumulator);
  *   2. the persistent main kernel: per KV tile, S, P, dV, dP, dS, dK and the
@@ -260,9 +260,10 @@ dab_status_t dab_bwd_preprocess(const void* o, const float* lse, const void* dou
 typedef struct {
     size_t status;   /* uint32 status word, uint32 error detail, uint32 counter */
     size_t sem;      /* uint32 [B*H][N][8][ways] semaphores                     */
-    size_t D;        /* float  [B*H*S]                                          */
-    size_t lse2;     /* float  [B*H*S] LSE * log2(e)                            */
-    size_t dqacc;    /* float  [ways][B*H*S][d]                                 */
+    size_t D;        /* float  [B*H*Spad], heads padded to whole 128-row tiles  */
+    size_t lse2;     /* float  [B*H*Spad] -LSE * log2(e), heads padded to tiles */
+    size_t dqacc;    /* float  [ways][B*H*Spad*d]: d = 128 row-major [row][d];
+                        d = 64 per 128-row tile [d/4][128][4]                  */
     size_t total;
 } dab_ws_layout_t;
 
