@@ -20,6 +20,7 @@ namespace dab {
 template <int HD> int bwd_smem_bytes();
 template <int HD> const void* bwd_kernel_ptr(bool ragged);
 int fwd_threads();
+int fwd_ctas(int BH, int N);
 template <int HD> int fwd_smem_bytes();
 template <int HD> const void* fwd_kernel_ptr();
 template <int HD> int selftest_smem_bytes();
@@ -284,7 +285,7 @@ static dab_status_t fwd_impl(const void* q, const void* k, const void* v, void* 
   p.tiles = tiles;
   dab::WsHeader* hdr = static_cast<dab::WsHeader*>(workspace);
   if (hdr != nullptr && cudaMemsetAsync(hdr, 0, 16, stream) != cudaSuccess) return DAB_ERR_CUDA;
-  const dim3 grid((unsigned)(p.BH * p.N)), block((unsigned)dab::fwd_threads());
+  const dim3 grid((unsigned)dab::fwd_ctas(p.BH, p.N)), block((unsigned)dab::fwd_threads());
   void* args[] = {&p, &hdr};
   cudaError_t e;
   if (d == 128)

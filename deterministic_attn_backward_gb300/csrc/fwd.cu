@@ -1,20 +1,28 @@
 // fwd.cu -- attention forward for GB300 (sm_103a): O = softmax(scale Q K^T) V
 // and LSE, the inputs the backward pass consumes.
 //
-// One CTA per (head, 128-row Q tile), two passes over the visible KV tiles:
-//   pass 1: S = Q K_c^T on the tensor cores; per Q row the maximum and the
-//           sum of exp2(scale*log2(e) S - max) (online update) -> LSE;
-//   pass 2: S again, P = exp2(scale*log2(e) S - LSE*log2(e)) in bf16 written
-//           over the S columns just read, O += P V_c on the tensor cores.
-// Recomputing S once avoids rescaling the O accumulator.  S is double
-// buffered in tensor memory, so the tensor cores compute the next tile's S
-// while the softmax warps work on the current one.  Two softmax warpgroups
-// take 64 key columns of every tile each (thread = Q row); their running
-// (max, sum) pairs are combined once, through shared memory, at the end of
-// pass 1.
-// With a block mask, KV tiles whose flag is zero are skipped by every role;
-// a Q tile with no visible KV tile gets O = 0 and LSE = -infinity.
-// Warps: 0 TMA producer, 1 MMA issuer, 4-11 softmax.
+// One pass over the visible KV tiles with an online softmax.  A CTA owns two
+// 128-row Q tiles of one head, A = 2p and B = 2p + 1 (B absent when the head
+// has an odd number of tiles), and walks the KV tiles either of them sees; K
+// and V are loaded once for both.  Per Q tile X and KV tile c the tensor
+// cores compute S_X = Q_X K_c^T into tensor memory, the softmax warpgroup of
+// X turns it into P (bf16, written over the S columns) and the tensor cores
+// accumulate O_X += P V_c in tensor memory.  The two Q tiles alternate on the
+// tensor cores, so the softmax of one overlaps the products of the other.
+//
+// Online softmax (thread = Q row, all 128 key columns of the tile): the row
+// keeps m, the running maximum used as the exponent offset, and l, the sum
+// of exp2(x - m) over the keys so far (x = scale*log2(e) * s).  When a tile
+// raises the row maximum by more than kRescale (in log2 units) or m is still
+// -infinity, the thread rescales its O row and l by exp2(m - m_new) and takes
+// m = m_new; otherwise P may exceed 1 by up to 2^kRescale, which bf16 and the
+// f32 accumulators hold without loss.  O and l share the scale history, so
+// O / l and LSE = (m + log2 l) ln 2 are exact up to rounding.
+//
+// Warps: 0 TMA producer, 1 MMA issuer, 4-7 softmax of Q tile A, 8-11 softmax
+// of Q tile B.  Tensor memory: S_A 0-127, S_B 128-255, O_A and O_B from 256.
+// With a block mask each Q tile skips the KV tiles its flags hide; a Q tile
+// with no visible KV tile gets O = 0 and LSE = -infinity.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -30,29 +38,25 @@ __device__ WsHeader g_fwd_status;  // status word when the caller gives no works
 namespace {
 
 constexpr int kFwdThreads = 384;
-constexpr int kFwdSoftmaxWarp0 = 4;  // warps 4-7: key columns 0-63, 8-11: 64-127
+constexpr int kFwdSoftmaxWarp0 = 4;  // warps 4-7: Q tile A, warps 8-11: Q tile B
 constexpr int kFwdSoftmaxWarps = 8;
-// The barrier counts (s_free, p_full) and the named barrier of the (max, sum)
-// combine expect exactly these warps: the block must hold all of them.
 static_assert(kFwdThreads == 32 * (kFwdSoftmaxWarp0 + kFwdSoftmaxWarps), "forward warp roles");
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescale = 8.0f;     // log2 units: P stays below 2^8
 
 template <int HD>
 struct FCfg {
   static constexpr int kTileBytes = kTile * HD * 2;
   static constexpr int kBlockBytes = kTile * 128;
-  static constexpr int kOffQ = 0;
-  static constexpr int kStages = 3;              // K, V tiles in flight
-  static constexpr int kOffK = kTileBytes;       // kStages stages
-  static constexpr int kOffV = (1 + kStages) * kTileBytes;
-  static constexpr int kOffBar = (1 + 2 * kStages) * kTileBytes;
+  static constexpr int kStages = (HD == 128) ? 2 : 3;  // K, V tiles in flight
+  static constexpr int kOffQ = 0;                       // Q_A, Q_B
+  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffV = (2 + kStages) * kTileBytes;
+  static constexpr int kOffBar = (2 + 2 * kStages) * kTileBytes;
   static constexpr int kOffMisc = kOffBar + 256;
-  static constexpr int kOffStat = kOffMisc + 16;  // [2 warpgroups][128 rows] (max, sum)
-  static constexpr int kSmemBytes = kOffStat + 2 * 128 * 8;
-  // Tensor memory: two S buffers (P written over the S columns just read),
-  // then the O accumulator.
-  static constexpr uint32_t kColS = 0;             // buffer b at kColS + 128 b
-  static constexpr uint32_t kColO = 256;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static constexpr uint32_t kColS = 0;                  // Q tile x at kColS + 128 x
+  static constexpr uint32_t kColO = 256;                // Q tile x at kColO + HD x
   static constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);   // S = Q K^T
   static constexpr uint32_t kIdO = idesc_bf16(128, HD, 0, 1);    // O += P V
 };
@@ -60,13 +64,21 @@ struct FCfg {
 struct FBars {
   uint64_t q_full;
   uint64_t kv_full[3], kv_empty[3];
-  uint64_t s_full[2];   // S of a tile in buffer b (MMA commit)
-  uint64_t s_free[2];   // pass 1: the softmax warps have read buffer b
-  uint64_t p_full[2];   // pass 2: P written over buffer b
-  uint64_t o_done[2];   // pass 2: P V of buffer b completed
-  uint64_t o_full, drain;
+  uint64_t s_full[2];   // S of Q tile x (MMA commit)
+  uint64_t p_full[2];   // P of Q tile x written (softmax warps)
+  uint64_t o_done[2];   // P V of Q tile x completed (MMA commit)
+  uint64_t drain;
 };
 static_assert(sizeof(FBars) <= 256, "barrier block");
+
+// The CTA's pair of Q tiles: CTAs are ordered longest causal range first.
+__device__ __forceinline__ void fwd_pair(const FwdParams& p, int& bh, int& qa, int& nq) {
+  const int npairs = (p.N + 1) / 2;
+  const int pr = npairs - 1 - (int)(blockIdx.x / p.BH);
+  bh = (int)(blockIdx.x % p.BH);
+  qa = 2 * pr;
+  nq = (qa + 1 < p.N) ? 2 : 1;
+}
 
 template <int HD>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p,
@@ -76,7 +88,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   FBars* bars = reinterpret_cast<FBars*>(smem + C::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + C::kOffMisc + 4);
-  float2* stat = reinterpret_cast<float2*>(smem + C::kOffStat);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (hdr == nullptr) hdr = &g_fwd_status;
@@ -84,10 +95,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     if (threadIdx.x == 0) raise_error(hdr, kStatusBounds, kDetailAlign);
     return;
   }
-  const int bh = blockIdx.x / p.N, qi = blockIdx.x % p.N;
-  const int nkv = (p.mask == kMaskCausal) ? qi + 1 : p.N;
-  // KV tile c takes part unless the block mask hides it (uniform per CTA)
-  auto visible = [&](int c) { return p.tiles == nullptr || p.tiles[(size_t)qi * p.N + c] != 0; };
+  int bh, qa, nq;
+  fwd_pair(p, bh, qa, nq);
+  const bool causal = (p.mask == kMaskCausal);
+  // KV tiles the CTA walks: those either Q tile may see
+  const int nkv = causal ? qa + nq : p.N;
+  // does Q tile x (0: A, 1: B) see KV tile c
+  auto sees = [&](int x, int c) {
+    const int qi = qa + x;
+    if (x >= nq) return false;
+    if (causal && c > qi) return false;
+    return p.tiles == nullptr || p.tiles[(size_t)qi * p.N + c] != 0;
+  };
+  auto any = [&](int c) { return sees(0, c) || sees(1, c); };
   const unsigned long long timeout = 2000000000ull;
 
   if (threadIdx.x == 0) {
@@ -96,13 +116,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], kFwdSoftmaxWarps);
-      mbar_init(&bars->p_full[s], kFwdSoftmaxWarps);
-      mbar_init(&bars->o_done[s], 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars->s_full[x], 1);
+      mbar_init(&bars->p_full[x], 4);
+      mbar_init(&bars->o_done[x], 1);
     }
-    mbar_init(&bars->o_full, 1);
     mbar_init(&bars->drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -118,35 +136,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   const WaitCtl wc{abort_flag, hdr, timeout};
 
   if (warp == 0) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&p.tm_q);
       prefetch_tensormap(&p.tm_k);
       prefetch_tensormap(&p.tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
-      const int qrow = bh * p.S + qi * kTile;
+      mbar_arrive_expect_tx(&bars->q_full, nq * C::kTileBytes);
+      for (int x = 0; x < nq; ++x) {
+        const int qrow = bh * p.S + (qa + x) * kTile;
 #pragma unroll
-      for (int db = 0; db < HD / 64; ++db)
-        tma_load_2d(smem + C::kOffQ + db * C::kBlockBytes, &p.tm_q, &bars->q_full, db * 64, qrow);
+        for (int db = 0; db < HD / 64; ++db)
+          tma_load_2d(smem + C::kOffQ + x * C::kTileBytes + db * C::kBlockBytes, &p.tm_q, &bars->q_full,
+                      db * 64, qrow);
+      }
       int it = 0, issued[C::kStages] = {};
-      bool ok = true;
-      for (int pass = 0; pass < 2 && ok; ++pass) {
-        for (int c = 0; c < nkv; ++c) {
-          if (!visible(c)) continue;
-          const int st = it % C::kStages;
-          if (it >= C::kStages && !mbar_wait(&bars->kv_empty[st], ((it / C::kStages) - 1) & 1, wc, 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->kv_full[st], (pass == 0 ? 1 : 2) * C::kTileBytes);
-          const int krow = bh * p.S + c * kTile;
+      for (int c = 0; c < nkv; ++c) {
+        if (!any(c)) continue;
+        const int st = it % C::kStages;
+        if (it >= C::kStages && !mbar_wait(&bars->kv_empty[st], ((it / C::kStages) - 1) & 1, wc, 1)) break;
+        mbar_arrive_expect_tx(&bars->kv_full[st], 2 * C::kTileBytes);
+        const int krow = bh * p.S + c * kTile;
 #pragma unroll
-          for (int db = 0; db < HD / 64; ++db) {
-            tma_load_2d(smem + C::kOffK + st * C::kTileBytes + db * C::kBlockBytes, &p.tm_k,
-                        &bars->kv_full[st], db * 64, krow);
-            if (pass == 1)
-              tma_load_2d(smem + C::kOffV + st * C::kTileBytes + db * C::kBlockBytes, &p.tm_v,
-                          &bars->kv_full[st], db * 64, krow);
-          }
-          ++issued[st];
-          ++it;
+        for (int db = 0; db < HD / 64; ++db) {
+          tma_load_2d(smem + C::kOffK + st * C::kTileBytes + db * C::kBlockBytes, &p.tm_k, &bars->kv_full[st],
+                      db * 64, krow);
+          tma_load_2d(smem + C::kOffV + st * C::kTileBytes + db * C::kBlockBytes, &p.tm_v, &bars->kv_full[st],
+                      db * 64, krow);
         }
+        ++issued[st];
+        ++it;
       }
       drain_wait(&bars->q_full, 0, hdr, timeout, 11);
       for (int st = 0; st < C::kStages; ++st)
@@ -154,202 +172,195 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // Per KV tile c (the CTA's it-th): for each Q tile x that sees c, P V of
+    // x, then, once that product has read P (it lies over S_x), S of x's
+    // next tile when that is c + 1 (a later one is issued at the start of
+    // its own iteration).  The products of A and B alternate on the tensor
+    // cores, so one tile's softmax runs while the other's products do.
     if (lane == 0) {
-      // Tile `it` (counted over both passes) uses KV stage and S buffer it & 1.
-      // Before S overwrites a buffer, its previous use must be finished: the
-      // softmax read it (pass 1: s_free) or P V read the P written over it
-      // (pass 2: o_done).  In pass 2, S of the next tile is issued before P V
-      // of the current one, so the tensor cores compute it while the softmax
-      // warps form P.
-      const uint32_t sQ = sbase + C::kOffQ;
+      const uint32_t tS[2] = {tbase + C::kColS, tbase + C::kColS + 128u};
+      const uint32_t tO[2] = {tbase + C::kColO, tbase + C::kColO + (uint32_t)HD};
+      int cnt[2] = {0, 0};        // P V issued per Q tile
+      bool s_ready[2] = {false, false};  // S of the tile x is about to process is issued
       bool ok = mbar_wait(&bars->q_full, 0, wc, 20);
+      auto issue_s = [&](int x, int c, int st) {
+        const uint32_t sQ = sbase + C::kOffQ + x * C::kTileBytes;
+        const uint32_t sK = sbase + C::kOffK + st * C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(tS[x], desc_kmajor(sQ, k, 128), desc_kmajor(sK, k, 128), C::kIdS, k > 0);
+        mma_commit(&bars->s_full[x]);
+      };
       int it = 0;
-      int last_pass[2] = {-1, -1}, uses[2][2] = {{0, 0}, {0, 0}};  // uses[pass][buffer]
-      int prev_it = -1;    // pass 2: the tile whose P V is still to issue
-      int first2 = 0;      // index of the first pass-2 tile (its P V starts O)
-      for (int pass = 0; pass < 2 && ok; ++pass) {
-        if (pass == 1) first2 = it;
-        for (int c = 0; c < nkv; ++c) {
-          if (!visible(c)) continue;
-          const int b = it & 1, st = it % C::kStages;
-          const uint32_t sK = sbase + C::kOffK + st * C::kTileBytes;
-          if (!mbar_wait(&bars->kv_full[st], (it / C::kStages) & 1, wc, 21)) { ok = false; break; }
-          if (last_pass[b] == 0 && !mbar_wait(&bars->s_free[b], (uses[0][b] - 1) & 1, wc, 22)) { ok = false; break; }
-          if (last_pass[b] == 1 && !mbar_wait(&bars->o_done[b], (uses[1][b] - 1) & 1, wc, 23)) { ok = false; break; }
+      for (int c = 0; c < nkv && ok; ++c) {
+        if (!any(c)) continue;
+        const int st = it % C::kStages;
+        if (!mbar_wait(&bars->kv_full[st], (it / C::kStages) & 1, wc, 21)) { ok = false; break; }
+        tc_fence_after();
+        for (int x = 0; x < 2; ++x) {
+          if (!sees(x, c) || s_ready[x]) continue;
+          // S_x is free once the previous P V of x has completed
+          if (cnt[x] > 0 && !mbar_wait(&bars->o_done[x], (cnt[x] - 1) & 1, wc, 22)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t tS = tbase + C::kColS + 128u * b;
-#pragma unroll
-          for (int k = 0; k < HD / 16; ++k)
-            mma_ss(tS, desc_kmajor(sQ, k, 128), desc_kmajor(sK, k, 128), C::kIdS, k > 0);
-          mma_commit(&bars->s_full[b]);
-          last_pass[b] = pass;
-          ++uses[pass][b];
-          if (pass == 0) mma_commit(&bars->kv_empty[st]);
-          if (pass == 1 && prev_it >= 0) {  // P V of the previous tile
-            const int pb = prev_it & 1;
-            if (!mbar_wait(&bars->p_full[pb], (uses[1][pb] - 1) & 1, wc, 24)) { ok = false; break; }
-            tc_fence_after();
-            const int pst = prev_it % C::kStages;
-            const uint32_t sV = sbase + C::kOffV + pst * C::kTileBytes;
-            const uint32_t tP = tbase + C::kColS + 128u * pb;
-#pragma unroll
-            for (int k = 0; k < kTile / 16; ++k)
-              mma_ts(tbase + C::kColO, tP + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(sV, k, 128),
-                     C::kIdO, !(prev_it == first2 && k == 0));
-            mma_commit(&bars->o_done[pb]);
-            mma_commit(&bars->kv_empty[pst]);
-          }
-          if (pass == 1) prev_it = it;
-          ++it;
+          issue_s(x, c, st);
         }
-      }
-      if (ok && prev_it >= 0) {  // P V of the last tile
-        const int pb = prev_it & 1;
-        if (mbar_wait(&bars->p_full[pb], (uses[1][pb] - 1) & 1, wc, 25)) {
+        if (!ok) break;
+        for (int x = 0; x < 2; ++x) {
+          if (!sees(x, c)) continue;
+          if (!mbar_wait(&bars->p_full[x], cnt[x] & 1, wc, 23)) { ok = false; break; }
           tc_fence_after();
-          const int pst = prev_it % C::kStages;
-          const uint32_t sV = sbase + C::kOffV + pst * C::kTileBytes;
-          const uint32_t tP = tbase + C::kColS + 128u * pb;
+          const uint32_t sV = sbase + C::kOffV + st * C::kTileBytes;
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_ts(tbase + C::kColO, tP + (k >> 2) * 64 + (k & 3) * 8, desc_mnmajor(sV, k, 128), C::kIdO,
-                   !(prev_it == first2 && k == 0));
-          mma_commit(&bars->o_done[pb]);
-          mma_commit(&bars->kv_empty[pst]);
-        } else {
-          ok = false;
+            mma_ts(tO[x], tS[x] + k * 8, desc_mnmajor(sV, k, 128), C::kIdO, (cnt[x] > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bars->o_done[x]);
+          ++cnt[x];
+          s_ready[x] = false;
+          // S of x's next tile right away when it is c + 1 (its K is loaded
+          // or on its way: the stage of c + 1 was freed by iteration c - 1)
+          if (c + 1 < nkv && sees(x, c + 1) && any(c + 1)) {
+            const int st1 = (it + 1) % C::kStages;
+            if (!mbar_wait(&bars->kv_full[st1], ((it + 1) / C::kStages) & 1, wc, 24)) { ok = false; break; }
+            if (!mbar_wait(&bars->o_done[x], (cnt[x] - 1) & 1, wc, 25)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(x, c + 1, st1);
+            s_ready[x] = true;
+          }
         }
+        if (!ok) break;
+        mma_commit(&bars->kv_empty[st]);
+        ++it;
       }
-      if (ok) mma_commit(&bars->o_full);
       mma_commit(&bars->drain);
       drain_wait(&bars->drain, 0, hdr, timeout, 13);
     }
     __syncwarp();
   } else if (warp >= kFwdSoftmaxWarp0) {
-    // Softmax: warpgroup h takes key columns 64 h .. 64 h + 63 of every tile;
-    // thread = Q row r of the tile.
-    const int h = (warp - kFwdSoftmaxWarp0) >> 2;
+    // ------------------------------------------------------------ softmax
+    // Warpgroup x owns Q tile x; thread = Q row r, all 128 key columns.
+    const int x = (warp - kFwdSoftmaxWarp0) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
+    const int qi = qa + x;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const bool causal = (p.mask == kMaskCausal);
+    const uint32_t tS = tbase + lane_off + C::kColS + 128u * x;
+    const uint32_t tO = tbase + lane_off + C::kColO + (uint32_t)HD * x;
     float m = -INFINITY, l = 0.f;
-    int it = 0, nvis = 0;
-    bool ok = true;
+    int cnt = 0;
+    bool ok = (x < nq);
+    const unsigned long long c2 = f32x2_pack(p.scale_log2e, p.scale_log2e);
     for (int c = 0; c < nkv && ok; ++c) {
-      if (!visible(c)) continue;
-      ++nvis;
-      const int b = it & 1;
-      if (!warp_wait(&bars->s_full[b], (it >> 1) & 1, wc, 30)) { ok = false; break; }
+      if (!sees(x, c)) continue;
+      if (!warp_wait(&bars->s_full[x], cnt & 1, wc, 30)) { ok = false; break; }
       tc_fence_after();
+      // x = scale*log2(e) * s for the 128 keys (all four loads in flight
+      // before one wait), -infinity where hidden: keys after the query on the
+      // causal diagonal tile, keys past S on a partial last tile
+      uint32_t v[128];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_off + C::kColS + 128u * b + 64 * h + 32 * ch, v);
-        float x[32];
-        float cmax = -INFINITY;
-        // masks apply only on the causal diagonal tile and a partial last tile
-        const bool masked = (causal && c == qi) || (c + 1) * kTile > p.S;
+      for (int ch = 0; ch < 4; ++ch) tmem_ld32_nowait(tS + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * ch]));
+      tmem_ld_wait();
+      const bool masked = (causal && c == qi) || (c + 1) * kTile > p.S;
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 128; e += 2) {
+        float a, b;
+        f32x2_unpack(mul_f32x2(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), c2), a, b);
         if (masked) {
+          if ((causal && c == qi && e > r) || c * kTile + e >= p.S) a = -INFINITY;
+          if ((causal && c == qi && e + 1 > r) || c * kTile + e + 1 >= p.S) b = -INFINITY;
+        }
+        v[e] = __float_as_uint(a);
+        v[e + 1] = __float_as_uint(b);
+        mx[(e >> 1) & 7] = fmaxf(mx[(e >> 1) & 7], fmaxf(a, b));
+      }
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // rescale when the maximum grew past the allowance (warp-uniform: the
+      // tensor-memory accesses are warp-collective; a lane that does not need
+      // it rescales by its own factor, which is also exact)
+      const bool need = (mt > m + kRescale) || (m == -INFINITY && mt != -INFINITY);
+      if (__any_sync(0xffffffffu, need)) {
+        const float mn = fmaxf(m, mt);
+        const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+        l *= alpha;
+        if (cnt > 0) {
+          // P V of the previous tile completed before S of this one was
+          // issued (the S columns held its P), so O is stable here
+          const unsigned long long a2 = f32x2_pack(alpha, alpha);
+#pragma unroll 1
+          for (int ch = 0; ch < HD / 8; ++ch) {
+            uint32_t o[8];
+            tmem_ld8(tO + 8 * ch, o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = 64 * h + 32 * ch + e;
-            x[e] = __uint_as_float(v[e]) * p.scale_log2e;
-            if (causal && c == qi && col > r) x[e] = -INFINITY;
-            if (c * kTile + col >= p.S) x[e] = -INFINITY;   // past the end of a partial last tile
-            cmax = fmaxf(cmax, x[e]);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            x[e] = __uint_as_float(v[e]) * p.scale_log2e;
-            cmax = fmaxf(cmax, x[e]);
+            for (int e = 0; e < 8; e += 2) {
+              float a, b;
+              f32x2_unpack(mul_f32x2(f32x2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), a, b);
+              o[e] = __float_as_uint(a);
+              o[e + 1] = __float_as_uint(b);
+            }
+            tmem_st8(tO + 8 * ch, o);
           }
         }
-        // A half row may have seen no visible key yet (its keys all masked):
-        // then the sum stays exactly 0 (no -inf - -inf).
-        const float mn = fmaxf(m, cmax);
-        const float base = (mn == -INFINITY) ? 0.f : mn;
-        float sum = 0.f;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) sum += ex2_approx(x[e] - base);
-        l = l * ex2_approx(m - base) + sum;
-        m = mn;
+        if (mn != -INFINITY) m = mn;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_free[b]);
-      ++it;
-    }
-    // Combine the two warpgroups' (max, sum) of each row.  Every softmax warp
-    // reaches this barrier, also after a failed wait.
-    stat[h * 128 + r] = make_float2(m, l);
-    named_bar_sync(1, 32 * kFwdSoftmaxWarps);
-    const float2 s0 = stat[r], s1 = stat[128 + r];
-    const float mt = fmaxf(s0.x, s1.x);
-    float lse2 = -INFINITY;
-    if (mt != -INFINITY) {
-      const float lt = s0.y * ex2_approx(s0.x - mt) + s1.y * ex2_approx(s1.x - mt);
-      lse2 = mt + __log2f(lt);
-    }
-    for (int c = 0; c < nkv && ok; ++c) {
-      if (!visible(c)) continue;
-      const int b = it & 1;
-      if (!warp_wait(&bars->s_full[b], (it >> 1) & 1, wc, 31)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t tS = tbase + lane_off + C::kColS + 128u * b + 64 * h;
+      // P = exp2(x - m) (a hidden key gives exp2(-inf) = 0), in bf16 over
+      // the S columns: keys 32 ch .. 32 ch + 31 -> columns 16 ch .. 16 ch + 15
+      const float mb = (m == -INFINITY) ? 0.f : m;
+      const unsigned long long nm2 = f32x2_pack(-mb, -mb);
+      float sm[8];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tS + 32 * ch, v);
+      for (int i = 0; i < 8; ++i) sm[i] = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
         uint32_t w16[16];
-        const bool masked = (causal && c == qi) || (c + 1) * kTile > p.S;
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int col = 64 * h + 32 * ch + e;
-          float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), p.scale_log2e, -lse2));
-          float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), p.scale_log2e, -lse2));
-          if (masked) {
-            if (causal && c == qi) {
-              if (col > r) p0 = 0.f;
-              if (col + 1 > r) p1 = 0.f;
-            }
-            if (c * kTile + col >= p.S) p0 = 0.f;
-            if (c * kTile + col + 1 >= p.S) p1 = 0.f;
-          }
+          float a, b;
+          f32x2_unpack(add_f32x2(f32x2_pack(__uint_as_float(v[32 * ch + e]), __uint_as_float(v[32 * ch + e + 1])), nm2),
+                       a, b);
+          const float p0 = ex2_approx(a), p1 = ex2_approx(b);
+          sm[(e >> 1) & 7] += p0 + p1;
           w16[e >> 1] = pack_bf16x2(p0, p1);
         }
-        // P over the columns this thread has read (packed: 16 words per 32 keys)
         tmem_st16_nowait(tS + 16 * ch, w16);
       }
+      const float sum0 = (sm[0] + sm[1]) + (sm[2] + sm[3]), sum1 = (sm[4] + sm[5]) + (sm[6] + sm[7]);
+      l += sum0 + sum1;
       tmem_st_wait_all();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[b]);
-      ++it;
+      if (lane == 0) mbar_arrive(&bars->p_full[x]);
+      ++cnt;
     }
-    if (ok && warp_wait(&bars->o_full, 0, wc, 33)) {
-      tc_fence_after();
-      const size_t row = (size_t)bh * p.S + (size_t)qi * kTile + r;
-      const bool row_in = qi * kTile + r < p.S;  // rows of a partial last tile
+    if (ok || x >= nq) {
+      if (x < nq && (cnt == 0 || warp_wait(&bars->o_done[x], (cnt - 1) & 1, wc, 33))) {
+        tc_fence_after();
+        const size_t row = (size_t)bh * p.S + (size_t)qi * kTile + r;
+        const bool row_in = qi * kTile + r < p.S;  // rows of a partial last tile
+        const float inv = (cnt > 0 && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
-      for (int ch = 0; ch < HD / 64; ++ch) {    // this warpgroup's half of the O columns
-        const int col0 = h * (HD / 2) + 32 * ch;
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_off + C::kColO + col0, v);
-        if (nvis == 0) {  // nothing visible: O = 0 (the accumulator was never written)
+        for (int ch = 0; ch < HD / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * ch, o);
+          if (cnt == 0) {  // nothing visible: O = 0 (the accumulator was never written)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0u;
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.o + row * HD + 32 * ch);
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm)
+            if (row_in)
+              dst[mm] = make_uint4(pack_bf16x2(inv * __uint_as_float(o[8 * mm]), inv * __uint_as_float(o[8 * mm + 1])),
+                                   pack_bf16x2(inv * __uint_as_float(o[8 * mm + 2]), inv * __uint_as_float(o[8 * mm + 3])),
+                                   pack_bf16x2(inv * __uint_as_float(o[8 * mm + 4]), inv * __uint_as_float(o[8 * mm + 5])),
+                                   pack_bf16x2(inv * __uint_as_float(o[8 * mm + 6]), inv * __uint_as_float(o[8 * mm + 7])));
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.o + row * HD + col0);
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm)
-          if (row_in) dst[mm] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * mm]), __uint_as_float(v[8 * mm + 1])),
-                               pack_bf16x2(__uint_as_float(v[8 * mm + 2]), __uint_as_float(v[8 * mm + 3])),
-                               pack_bf16x2(__uint_as_float(v[8 * mm + 4]), __uint_as_float(v[8 * mm + 5])),
-                               pack_bf16x2(__uint_as_float(v[8 * mm + 6]), __uint_as_float(v[8 * mm + 7])));
+        if (row_in) p.lse[row] = (cnt > 0 && l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
       }
-      if (row_in && h == 0) p.lse[row] = lse2 * kLn2;
     }
   }
   tc_fence_before();
@@ -363,6 +374,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 }  // namespace
 
 int fwd_threads() { return kFwdThreads; }
+int fwd_ctas(int BH, int N) { return BH * ((N + 1) / 2); }
 
 template <int HD>
 int fwd_smem_bytes() {
