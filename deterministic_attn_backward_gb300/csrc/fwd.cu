@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           tma_load_2d(smem + C::kOffQ + x * C::kTileBytes + db * C::kBlockBytes, &p.tm_q, &bars->q_full,
                       db * 64, qrow);
       }
-      int it = 0, issued[C::kStages] = {};
+      int it = 0;
       for (int c = 0; c < nkv; ++c) {
         if (!any(c)) continue;
         const int st = it % C::kStages;
@@ -163,12 +163,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           tma_load_2d(smem + C::kOffV + st * C::kTileBytes + db * C::kBlockBytes, &p.tm_v, &bars->kv_full[st],
                       db * 64, krow);
         }
-        ++issued[st];
         ++it;
       }
       drain_wait(&bars->q_full, 0, hdr, timeout, 11);
-      for (int st = 0; st < C::kStages; ++st)
-        if (issued[st] > 0) drain_wait(&bars->kv_full[st], (issued[st] - 1) & 1, hdr, timeout, 12);
+      // stage st took loads it' = st, st + kStages, ... < it
+#pragma unroll
+      for (int st = 0; st < C::kStages; ++st) {
+        const int issued = (it - st + C::kStages - 1) / C::kStages;
+        if (issued > 0) drain_wait(&bars->kv_full[st], (issued - 1) & 1, hdr, timeout, 12);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -179,17 +182,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     // its own iteration).  The products of A and B alternate on the tensor
     // cores, so one tile's softmax runs while the other's products do.
     if (lane == 0) {
-      const uint32_t tS[2] = {tbase + C::kColS, tbase + C::kColS + 128u};
-      const uint32_t tO[2] = {tbase + C::kColO, tbase + C::kColO + (uint32_t)HD};
-      int cnt[2] = {0, 0};        // P V issued per Q tile
-      bool s_ready[2] = {false, false};  // S of the tile x is about to process is issued
+      // per Q tile x (scalars, not arrays, so that they stay in registers):
+      // P V products issued, and whether S of the tile x processes next is
+      // already issued
+      int cnt0 = 0, cnt1 = 0;
+      bool rdy0 = false, rdy1 = false;
       bool ok = mbar_wait(&bars->q_full, 0, wc, 20);
       auto issue_s = [&](int x, int c, int st) {
         const uint32_t sQ = sbase + C::kOffQ + x * C::kTileBytes;
         const uint32_t sK = sbase + C::kOffK + st * C::kTileBytes;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tS[x], desc_kmajor(sQ, k, 128), desc_kmajor(sK, k, 128), C::kIdS, k > 0);
+          mma_ss(tbase + C::kColS + 128u * x, desc_kmajor(sQ, k, 128), desc_kmajor(sK, k, 128), C::kIdS, k > 0);
         mma_commit(&bars->s_full[x]);
       };
       int it = 0;
@@ -198,34 +202,38 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         const int st = it % C::kStages;
         if (!mbar_wait(&bars->kv_full[st], (it / C::kStages) & 1, wc, 21)) { ok = false; break; }
         tc_fence_after();
+#pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if (!sees(x, c) || s_ready[x]) continue;
+          const int cx = x ? cnt1 : cnt0;
+          if (!sees(x, c) || (x ? rdy1 : rdy0)) continue;
           // S_x is free once the previous P V of x has completed
-          if (cnt[x] > 0 && !mbar_wait(&bars->o_done[x], (cnt[x] - 1) & 1, wc, 22)) { ok = false; break; }
+          if (cx > 0 && !mbar_wait(&bars->o_done[x], (cx - 1) & 1, wc, 22)) { ok = false; break; }
           tc_fence_after();
           issue_s(x, c, st);
         }
         if (!ok) break;
+#pragma unroll
         for (int x = 0; x < 2; ++x) {
           if (!sees(x, c)) continue;
-          if (!mbar_wait(&bars->p_full[x], cnt[x] & 1, wc, 23)) { ok = false; break; }
+          const int cx = x ? cnt1 : cnt0;
+          if (!mbar_wait(&bars->p_full[x], cx & 1, wc, 23)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sV = sbase + C::kOffV + st * C::kTileBytes;
+          const uint32_t tSx = tbase + C::kColS + 128u * x, tOx = tbase + C::kColO + (uint32_t)HD * x;
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_ts(tO[x], tS[x] + k * 8, desc_mnmajor(sV, k, 128), C::kIdO, (cnt[x] > 0 || k > 0) ? 1u : 0u);
+            mma_ts(tOx, tSx + k * 8, desc_mnmajor(sV, k, 128), C::kIdO, (cx > 0 || k > 0) ? 1u : 0u);
           mma_commit(&bars->o_done[x]);
-          ++cnt[x];
-          s_ready[x] = false;
+          if (x) { ++cnt1; rdy1 = false; } else { ++cnt0; rdy0 = false; }
           // S of x's next tile right away when it is c + 1 (its K is loaded
           // or on its way: the stage of c + 1 was freed by iteration c - 1)
           if (c + 1 < nkv && sees(x, c + 1) && any(c + 1)) {
             const int st1 = (it + 1) % C::kStages;
             if (!mbar_wait(&bars->kv_full[st1], ((it + 1) / C::kStages) & 1, wc, 24)) { ok = false; break; }
-            if (!mbar_wait(&bars->o_done[x], (cnt[x] - 1) & 1, wc, 25)) { ok = false; break; }
+            if (!mbar_wait(&bars->o_done[x], cx & 1, wc, 25)) { ok = false; break; }
             tc_fence_after();
             issue_s(x, c + 1, st1);
-            s_ready[x] = true;
+            if (x) rdy1 = true; else rdy0 = true;
           }
         }
         if (!ok) break;
@@ -265,17 +273,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+      // two copies of the loop, so that the tiles without hidden keys run
+      // straight-line code with no per-element test or branch
+      if (!masked) {
 #pragma unroll
-      for (int e = 0; e < 128; e += 2) {
-        float a, b;
-        f32x2_unpack(mul_f32x2(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), c2), a, b);
-        if (masked) {
-          if ((causal && c == qi && e > r) || c * kTile + e >= p.S) a = -INFINITY;
-          if ((causal && c == qi && e + 1 > r) || c * kTile + e + 1 >= p.S) b = -INFINITY;
+        for (int e = 0; e < 128; e += 2) {
+          float a, b;
+          f32x2_unpack(mul_f32x2(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), c2), a, b);
+          v[e] = __float_as_uint(a);
+          v[e + 1] = __float_as_uint(b);
+          mx[(e >> 1) & 7] = fmaxf(mx[(e >> 1) & 7], fmaxf(a, b));
         }
-        v[e] = __float_as_uint(a);
-        v[e + 1] = __float_as_uint(b);
-        mx[(e >> 1) & 7] = fmaxf(mx[(e >> 1) & 7], fmaxf(a, b));
+      } else {
+        const int lim = min((causal && c == qi) ? r + 1 : kTile, p.S - c * kTile);  // keys < lim visible
+#pragma unroll
+        for (int e = 0; e < 128; e += 2) {
+          float a, b;
+          f32x2_unpack(mul_f32x2(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), c2), a, b);
+          a = (e < lim) ? a : -INFINITY;
+          b = (e + 1 < lim) ? b : -INFINITY;
+          v[e] = __float_as_uint(a);
+          v[e + 1] = __float_as_uint(b);
+          mx[(e >> 1) & 7] = fmaxf(mx[(e >> 1) & 7], fmaxf(a, b));
+        }
       }
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
