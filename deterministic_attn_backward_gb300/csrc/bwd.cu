@@ -44,6 +44,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -621,45 +622,52 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         // are -LSE*log2(e), so each pair of columns is one packed fma.
         uint32_t pk[32];
         const unsigned long long c2 = f32x2_pack(p.scale_log2e, p.scale_log2e);
+        // the loop in two copies, so that off-diagonal steps run it with no
+        // per-element test or branch
+        auto p_phase = [&](auto diag_tag) {
+          constexpr bool kDiag = decltype(diag_tag)::value;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tbase + lane_off + C::kColS + 64 * h + 32 * c, v);
-          uint32_t w16[16];
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + lane_off + C::kColS + 64 * h + 32 * c, v);
+            uint32_t w16[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const int col = 32 * c + e;          // column within this half
-            const float4 l4 = *reinterpret_cast<const float4*>(lse + col);
-            float x0, x1, x2, x3;
-            f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), c2,
-                                   f32x2_pack(l4.x, l4.y)), x0, x1);
-            f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), c2,
-                                   f32x2_pack(l4.z, l4.w)), x2, x3);
-            float p0 = ex2_approx(x0);
-            float p1 = ex2_approx(x1);
-            float p2 = ex2_approx(x2);
-            float p3 = ex2_approx(x3);
-            if (diag) {
-              const int qc = 64 * h + col;       // Q column within the tile
-              if (r > qc) p0 = 0.f;
-              if (r > qc + 1) p1 = 0.f;
-              if (r > qc + 2) p2 = 0.f;
-              if (r > qc + 3) p3 = 0.f;
+            for (int e = 0; e < 32; e += 4) {
+              const int col = 32 * c + e;          // column within this half
+              const float4 l4 = *reinterpret_cast<const float4*>(lse + col);
+              float x0, x1, x2, x3;
+              f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), c2,
+                                     f32x2_pack(l4.x, l4.y)), x0, x1);
+              f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), c2,
+                                     f32x2_pack(l4.z, l4.w)), x2, x3);
+              float p0 = ex2_approx(x0);
+              float p1 = ex2_approx(x1);
+              float p2 = ex2_approx(x2);
+              float p3 = ex2_approx(x3);
+              if (kDiag) {
+                const int qc = 64 * h + col;       // Q column within the tile
+                p0 = (r > qc) ? 0.f : p0;
+                p1 = (r > qc + 1) ? 0.f : p1;
+                p2 = (r > qc + 2) ? 0.f : p2;
+                p3 = (r > qc + 3) ? 0.f : p3;
+              }
+              w16[e >> 1] = pack_bf16x2(p0, p1);
+              w16[(e >> 1) + 1] = pack_bf16x2(p2, p3);
+              pk[16 * c + (e >> 1)] = w16[e >> 1];
+              pk[16 * c + (e >> 1) + 1] = w16[(e >> 1) + 1];
             }
-            w16[e >> 1] = pack_bf16x2(p0, p1);
-            w16[(e >> 1) + 1] = pack_bf16x2(p2, p3);
-            pk[16 * c + (e >> 1)] = w16[e >> 1];
-            pk[16 * c + (e >> 1) + 1] = w16[(e >> 1) + 1];
-          }
-          if (tail_kv && key_out) {
+            if (tail_kv && key_out) {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-              w16[x] = 0u;
-              pk[16 * c + x] = 0u;
+              for (int x = 0; x < 16; ++x) {
+                w16[x] = 0u;
+                pk[16 * c + x] = 0u;
+              }
             }
+            tmem_st16_nowait(tbase + lane_off + C::kColS + 64 * h + 16 * c, w16);
           }
-          tmem_st16_nowait(tbase + lane_off + C::kColS + 64 * h + 16 * c, w16);
-        }
+        };
+        if (diag) p_phase(std::true_type{});
+        else p_phase(std::false_type{});
         tmem_st_wait_all();
         tc_fence_before();
         __syncwarp();
