@@ -815,6 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           if (!g) { ok = false; break; }
           if (p.plain_add && !store) fence_acq_rel_gpu();
         }
+        // one straight-line loop per kind of add (no per-element branch)
         if (HD == 128) {
           if (store) {
 #pragma unroll
@@ -833,31 +834,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
               for (int k = 0; k < 16; ++k)
                 if (c + k < nvalid) base[(size_t)(c + k) * HD] = a[k] + __uint_as_float(v[c + k]);
             }
-          } else {
+          } else if (deterministic) {
 #pragma unroll
             for (int q = 0; q < 64; ++q) {
               if (q < nvalid) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
-              // Ordered schedules: spread the adds out so that they do not
-              // fill the SM's memory-instruction queue in one burst (the
-              // softmax warps' shared-memory loads wait behind them).
-              if (deterministic && (q & 7) == 7) __nanosleep(20);
+              // spread the adds out so that they do not fill the SM's
+              // memory-instruction queue in one burst (the softmax warps'
+              // shared-memory loads wait behind them)
+              if ((q & 7) == 7) __nanosleep(20);
             }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 64; ++q)
+              if (q < nvalid) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
           }
         } else {
+          if (store) {
 #pragma unroll
-          for (int m = 0; m < kVals / 4; ++m) {
-            float* dst = base + (size_t)m * (kTile * 4);
-            const float a0 = __uint_as_float(v[4 * m]), a1 = __uint_as_float(v[4 * m + 1]);
-            const float a2 = __uint_as_float(v[4 * m + 2]), a3 = __uint_as_float(v[4 * m + 3]);
-            if (store) {
-              *reinterpret_cast<float4*>(dst) = make_float4(a0, a1, a2, a3);
-            } else if (deterministic && p.plain_add) {
-              // load + add + store: the same IEEE adds in the same order
+            for (int m = 0; m < kVals / 4; ++m)
+              *reinterpret_cast<float4*>(base + (size_t)m * (kTile * 4)) =
+                  make_float4(__uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
+                              __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
+          } else if (deterministic && p.plain_add) {
+            // load + add + store: the same IEEE adds in the same order
+#pragma unroll
+            for (int m = 0; m < kVals / 4; ++m) {
+              float* dst = base + (size_t)m * (kTile * 4);
               const float4 b = ld_cg_v4_f32(dst);
-              *reinterpret_cast<float4*>(dst) = make_float4(b.x + a0, b.y + a1, b.z + a2, b.w + a3);
-            } else {
-              red_add_v4_f32(dst, a0, a1, a2, a3);
+              *reinterpret_cast<float4*>(dst) =
+                  make_float4(b.x + __uint_as_float(v[4 * m]), b.y + __uint_as_float(v[4 * m + 1]),
+                              b.z + __uint_as_float(v[4 * m + 2]), b.w + __uint_as_float(v[4 * m + 3]));
             }
+          } else {
+#pragma unroll
+            for (int m = 0; m < kVals / 4; ++m)
+              red_add_v4_f32(base + (size_t)m * (kTile * 4), __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
+                             __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
           }
         }
         if (deterministic) {
