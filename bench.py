@@ -34,13 +34,18 @@ SEED, QK_SCALE = 2, 0.5
 ALL_SCHEDS = ("serial", "descending_q", "shift", "atomic")
 DET_SCHEDS = ("serial", "descending_q", "shift")
 
-# DRAM bytes (read + write) of one main-kernel launch of this workload, from
-# ncu captures of B=1 launches of the same kernel (traffic scales with the
-# number of heads, so x2), keyed by the SHA-1 of the kernel source they were
-# taken on.  Reported only while the source is unchanged.
+# DRAM bytes (read + write, MB) of one main-kernel launch at B=1, H=16,
+# S=8192, d=128 per (mask, schedule), from ncu captures of that launch,
+# keyed by the SHA-1 of the kernel source they were taken on.  Traffic scales
+# with the number of heads, so the B=2 launch moves twice as much.  Reported
+# only while the source is unchanged.
 TRAFFIC_CAPTURES = {
-    # causal 390.2 + 350.2 MB, full 398.3 + 366.3 MB: mean of the masks, x2
-    "8ad21261094c8ef57599822e43538f7d083882b5": 2 * ((390.2 + 350.2) + (398.3 + 366.3)) / 2 * 1e6,
+    "cbca788546cba291a7f9ead4cfa106c034cf818b": {
+        "causal/serial": 468.7 + 407.8, "causal/descending_q": 393.1 + 353.1,
+        "causal/shift": 464.6 + 472.7, "causal/atomic": 202.8 + 88.4,
+        "full/serial": 398.8 + 361.7, "full/descending_q": 399.0 + 366.0,
+        "full/shift": 443.3 + 466.8, "full/atomic": 202.6 + 87.7,
+    },
 }
 MASKS = ("causal", "full")
 
@@ -66,13 +71,17 @@ def load_peaks() -> dict:
                 "source": "fallback"}
 
 
-def traffic_for_current_kernel():
+def traffic_for_current_kernel(scheds: dict):
+    """Mean DRAM bytes per launch of the timed launches (one per mask)."""
     import hashlib
     path = os.path.join(ROOT, "deterministic_attn_backward_gb300", "csrc", "bwd.cu")
     with open(path, "rb") as f:
         h = hashlib.sha1(f.read()).hexdigest()
-    t = TRAFFIC_CAPTURES.get(h)
-    return round(t) if t is not None else None
+    caps = TRAFFIC_CAPTURES.get(h, {})
+    per = [caps.get(f"{m}/{scheds[m]}") for m in MASKS]
+    if any(x is None for x in per):
+        return None
+    return round(2 * sum(per) / len(per) * 1e6)
 
 
 def max_over_ranks(value: float, world: int, device=None) -> float:
@@ -371,7 +380,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         "frac_of_peak": round(value / world / peak, 4),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic_for_current_kernel(),
+                     "traffic": traffic_for_current_kernel(step_scheds),
                      "kernel": "bwd_kernel<128>", "peak_source": peaks["source"] + " (burst)",
                      "launch_ms": {m: round(x, 4) for m, x in main_ms.items()}},
         "own_tensor_peak": {"tflops": round(own_peak["tflops"], 1),
