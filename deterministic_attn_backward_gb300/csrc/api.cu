@@ -18,7 +18,7 @@
 namespace dab {
 // kernels (bwd.cu, fwd.cu, aux.cu, selftest.cu)
 template <int HD> int bwd_smem_bytes();
-template <int HD> const void* bwd_kernel_ptr(bool ragged);
+template <int HD> const void* bwd_kernel_ptr(bool ragged, bool chunk_major);
 int fwd_threads();
 int fwd_ctas(int BH, int N);
 template <int HD> int fwd_smem_bytes();
@@ -31,7 +31,7 @@ int peak_threads();
 cudaError_t launch_preprocess(int HD, const void* o, const void* dout, const float* lse, float* D,
                               float* lse2, uint32_t* sem, int n_sem, WsHeader* hdr, float* dqacc,
                               long long dq_elems, int BH, int S, int S_pad, int grid, cudaStream_t stream);
-cudaError_t launch_convert(const float* dqacc, void* dq, int ntiles, float scale, long long acc_stride,
+cudaError_t launch_convert(const float* dqacc, int chunk_major, void* dq, int ntiles, float scale, long long acc_stride,
                            int ways, int causal, int N, int S, int d, int grid, const int* count,
                            cudaStream_t stream);
 cudaError_t launch_block_tables(const uint8_t* tiles, int N, int causal, int descending,
@@ -76,10 +76,11 @@ bool device_setup(int* dev_out, int* sms_out) {
     if (di.supported) {
       bool ok = true;
       for (bool ragged : {false, true}) {
-        ok &= cudaFuncSetAttribute(dab::bwd_kernel_ptr<64>(ragged), cudaFuncAttributeMaxDynamicSharedMemorySize,
+        ok &= cudaFuncSetAttribute(dab::bwd_kernel_ptr<64>(ragged, true), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    dab::bwd_smem_bytes<64>()) == cudaSuccess;
-        ok &= cudaFuncSetAttribute(dab::bwd_kernel_ptr<128>(ragged), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   dab::bwd_smem_bytes<128>()) == cudaSuccess;
+        for (bool cm : {false, true})
+          ok &= cudaFuncSetAttribute(dab::bwd_kernel_ptr<128>(ragged, cm), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     dab::bwd_smem_bytes<128>()) == cudaSuccess;
       }
       ok &= cudaFuncSetAttribute(dab::fwd_kernel_ptr<64>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  dab::fwd_smem_bytes<64>()) == cudaSuccess;
@@ -182,6 +183,14 @@ dab_status_t resolve_sched(dab_mask_t mask, int B, int H, int S, int ctas, dab_s
 }
 
 int acc_ways(dab_sched_t sched) { return sched == DAB_SCHED_ATOMIC ? 1 : dab::kAccWays; }
+
+// Layout of the f32 dQ accumulation tiles.  Chunk-major ([d/4][128 rows][4]
+// per 128-row tile: a warp's 16-byte adds of one chunk are 512 contiguous
+// bytes) for the ordered schedules and for d = 64.  The atomic schedule at
+// d = 128 keeps row-major [row][d] with one-float adds of whole rows: its
+// unpaced vector reds ran 3 % slower than scalar ones, while the ordered
+// schedules gain 1-2 % (8 % with DAB_BWD_PLAIN_ADD) from the vector form.
+int acc_chunk_major(int d, dab_sched_t sched) { return (d == 64 || sched != DAB_SCHED_ATOMIC) ? 1 : 0; }
 
 bool layout(int B, int H, int S, int d, dab_sched_t sched, dab_ws_layout_t* L) {
   if (check_shape(B, H, S, d) != DAB_OK) return false;
@@ -447,7 +456,8 @@ static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const 
   cudaError_t e = cudaSuccess;
   if (!(flags & DAB_BWD_SKIP_MAIN)) {
     const bool ragged = (S % 128) != 0;
-    e = cudaLaunchKernelExC(&cfg, d == 128 ? dab::bwd_kernel_ptr<128>(ragged) : dab::bwd_kernel_ptr<64>(ragged),
+    const bool cm = acc_chunk_major(d, sched) != 0;
+    e = cudaLaunchKernelExC(&cfg, d == 128 ? dab::bwd_kernel_ptr<128>(ragged, cm) : dab::bwd_kernel_ptr<64>(ragged, cm),
                             args);
     if (e != cudaSuccess) return cuda_fail(e, "main kernel launch");
   }
@@ -455,7 +465,7 @@ static dab_status_t bwd_impl(const void* q, const void* k, const void* v, const 
   if (!(flags & DAB_BWD_SKIP_CONVERT) && !p.fuse_convert) {
     const int ntiles = B * H * N;
     const int cgrid = ntiles < 8 * sms ? ntiles : 8 * sms;
-    e = dab::launch_convert(p.dqacc, dq, ntiles, scale, p.acc_stride, p.acc_ways,
+    e = dab::launch_convert(p.dqacc, acc_chunk_major(d, sched), dq, ntiles, scale, p.acc_stride, p.acc_ways,
                             mask == DAB_MASK_CAUSAL ? 1 : 0, N, S, d, cgrid,
                             block ? p.blk_count : nullptr, stream);
     if (e != cudaSuccess) return cuda_fail(e, "convert launch");

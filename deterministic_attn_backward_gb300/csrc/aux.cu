@@ -118,11 +118,11 @@ __global__ void __launch_bounds__(256) preprocess_kernel(
 // tile): N for the full mask, j + 1 for causal, the tables' count under a
 // block mask, 0 -> dQ = 0) are added in index order, times scale, rounded to
 // bf16 (RN-even): the arithmetic of the main kernel's tail, so both give the
-// same bits.  d = 128: row-major accumulator [B*H*S][d], 16-byte vectors.
-// d = 64: chunk-major tiles [d/4][128 rows][4] (every head padded to whole
-// tiles), read 16 bytes per thread over consecutive rows, staged in shared
-// memory and written row by row.
-template <int HD>
+// same bits.  kCM: chunk-major tiles [d/4][128 rows][4] (every head padded
+// to whole tiles), read 16 bytes per thread over consecutive rows, staged in
+// shared memory and written row by row.  Otherwise (atomic, d = 128):
+// row-major accumulator [B*H*S][d], 16-byte vectors.
+template <int HD, bool kCM>
 __global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__ acc,
                                                       __nv_bfloat16* __restrict__ dq, int ntiles,
                                                       float scale, long long acc_stride_vec4,
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__
                                                       const int* __restrict__ count) {
   constexpr int kChunks = HD / 4;
   constexpr int kRowBytes = HD * 2 + 16;
-  __shared__ __align__(16) uint8_t stage[(HD == 64) ? kTile * kRowBytes : 16];
+  __shared__ __align__(16) uint8_t stage[kCM ? kTile * kRowBytes : 16];
   for (int T = blockIdx.x; T < ntiles; T += gridDim.x) {
     const int bh = T / N, j = T % N;
     int nacc = ways < N ? ways : N;
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(256) convert_kernel(const float4* __restrict__
       if (c < nacc) nacc = c;
     }
     const int rows = min(kTile, S - j * kTile);
-    if constexpr (HD == 128) {
+    if constexpr (!kCM) {
       const size_t e0 = ((size_t)bh * S + (size_t)j * kTile) * HD;
       const float4* a = acc + e0 / 4;
       uint2* out = reinterpret_cast<uint2*>(dq + e0);
@@ -271,15 +271,18 @@ cudaError_t launch_status_collect(const uint32_t* slots, int n, void* hdr, cudaS
   return cudaGetLastError();
 }
 
-cudaError_t launch_convert(const float* dqacc, void* dq, int ntiles, float scale, long long acc_stride,
-                           int ways, int causal, int N, int S, int d, int grid, const int* count,
-                           cudaStream_t stream) {
+cudaError_t launch_convert(const float* dqacc, int chunk_major, void* dq, int ntiles, float scale,
+                           long long acc_stride, int ways, int causal, int N, int S, int d, int grid,
+                           const int* count, cudaStream_t stream) {
   const float4* a = reinterpret_cast<const float4*>(dqacc);
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(dq);
-  if (d == 128)
-    convert_kernel<128><<<grid, 256, 0, stream>>>(a, out, ntiles, scale, acc_stride / 4, ways, causal, N, S, count);
+  const long long st4 = acc_stride / 4;
+  if (d == 64)
+    convert_kernel<64, true><<<grid, 256, 0, stream>>>(a, out, ntiles, scale, st4, ways, causal, N, S, count);
+  else if (chunk_major)
+    convert_kernel<128, true><<<grid, 256, 0, stream>>>(a, out, ntiles, scale, st4, ways, causal, N, S, count);
   else
-    convert_kernel<64><<<grid, 256, 0, stream>>>(a, out, ntiles, scale, acc_stride / 4, ways, causal, N, S, count);
+    convert_kernel<128, false><<<grid, 256, 0, stream>>>(a, out, ntiles, scale, st4, ways, causal, N, S, count);
   return cudaGetLastError();
 }
 

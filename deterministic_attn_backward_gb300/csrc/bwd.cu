@@ -17,16 +17,16 @@
 // global memory by the reducer warps: for the deterministic schedules in the
 // fixed order rank(i, j) (technical summary section 1: a fixed accumulation
 // order for dQ), gated by per-(head, Q tile, eighth, buffer) semaphores; for
-// ATOMIC with unordered float adds.  d = 128: the partial is dQ^T (d on
-// tensor-memory lanes), a reducer thread holds one d index over 64 Q rows and
-// a warp's 32 consecutive d indices form one 128-byte segment of a row of the
-// row-major accumulator [B*H*S][d].  d = 64: the partial is dQ (Q rows on
-// lanes) and the accumulator is stored chunk-major per 128-row tile,
-// [d/4][128 rows][4] f32, so that a thread adds 16 bytes at a time and a
-// warp's 32 rows of a chunk form 512 contiguous bytes.  For the deterministic
-// schedules the same kernel then
-// converts dQ to bf16 in its tail: a CTA without units left converts the dQ
-// tiles whose semaphores show every contribution in.
+// ATOMIC with unordered float adds.  The partial is dQ (Q rows on
+// tensor-memory lanes) and the accumulator is stored chunk-major per 128-row
+// tile, [d/4][128 rows][4] f32, so that a thread adds 16 bytes at a time and
+// a warp's 32 rows of a chunk form 512 contiguous bytes.  The one exception,
+// ATOMIC at d = 128, keeps a row-major accumulator [B*H*S][d] with the
+// partial as dQ^T (d on lanes): a reducer thread holds one d index over 64 Q
+// rows and a warp's 32 one-float adds are one 128-byte segment of a row.  For
+// the deterministic schedules the same kernel then converts dQ to bf16 in
+// its tail: a CTA without units left converts the dQ tiles whose semaphores
+// show every contribution in.
 //
 // Warp roles (20 warps):
 //   warp 0      TMA producer (K_i, V_i per chain; Q_j, dO_j, LSE_j, D_j per
@@ -80,13 +80,10 @@ struct Cfg {
   static constexpr uint32_t kColDP = 2 * HD + 128;
   static constexpr uint32_t kColDQ = (HD == 128) ? kColDP : 384;  // d=128 reuses dP
   static constexpr int kChunks = HD / 4;                   // 16-byte chunks of a dQ row
-  // d = 64: chunk-major accumulator tiles [d/4][128][4]; d = 128: row-major.
-  static constexpr bool kChunkMajor = (HD == 64);
   // Instruction descriptors.
   static constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
   static constexpr uint32_t kIdAcc = idesc_bf16(128, HD, 0, 1);  // dV, dK
-  static constexpr uint32_t kIdDQ = (HD == 128) ? idesc_bf16(128, 128, 1, 1)   // dQ^T = K^T dS^T
-                                                : idesc_bf16(128, 64, 1, 1);   // dQ = dS K
+  static constexpr uint32_t kIdDQ = idesc_bf16(128, HD, 1, 1);  // dQ = dS K, or dQ^T = K^T dS^T (d = 128)
 };
 
 struct Bars {
@@ -182,9 +179,10 @@ static __device__ __noinline__ bool final_wait(const uint32_t* sem, uint32_t tar
 // been claimed by a running CTA before any tile is, and no unit waits for a
 // tile, so these waits always end.  The arithmetic is the convert pass's:
 // the buffers added in index order, times scale, rounded to bf16 (RN-even),
-// so dQ has the same bits whichever of the two wrote it.  A chunk-major tile
-// (d = 64) is read 16 bytes per thread (coalesced), the bf16 result goes
-// through shared memory (free once the roles are done) and out row by row.
+// so dQ has the same bits whichever of the two wrote it.  The ordered
+// schedules' tiles are chunk-major: read 16 bytes per thread (coalesced), the
+// bf16 result goes through shared memory (free once the roles are done) and
+// out row by row.
 template <int HD, bool kRagged>
 __device__ __forceinline__ void tail_convert(const BwdParams& p, Misc* misc, uint8_t* smem,
                                              const WaitCtl& wc) {
@@ -216,71 +214,36 @@ __device__ __forceinline__ void tail_convert(const BwdParams& p, Misc* misc, uin
     fence_acq_rel_gpu();
     // rows of the tile inside the head (a partial last tile stops at S)
     const int rows = kRagged ? min(kTile, p.S - j * kTile) : kTile;
-    if constexpr (HD == 128) {
-      // row-major accumulator: 16-byte vectors, two per thread and pass, all
-      // loads first, then the sums
-      const size_t e0 = ((size_t)bh * p.S + (size_t)j * kTile) * HD;
-      const float4* acc = reinterpret_cast<const float4*>(p.dqacc + e0);
-      uint2* out = reinterpret_cast<uint2*>(p.dq + e0);
-      const int n4 = rows * (HD / 4);
-      if (nacc == 0) {
-        for (int i = tid; i < n4; i += kThreads) out[i] = make_uint2(0u, 0u);
-      } else {
-        for (int i0 = tid; i0 < n4; i0 += 2 * kThreads) {
-          float4 w[2][kAccWays];
+    // chunk-major tile: chunk units u = chunk * 128 + row, consecutive
+    // threads on consecutive rows (coalesced 16-byte loads); the bf16
+    // result is staged in shared memory (free once the roles are done)
+    // and written row by row
+    const float4* acc = reinterpret_cast<const float4*>(p.dqacc) + ((size_t)bh * p.N + j) * (kTile * kChunks);
+    for (int u = tid; u < kTile * kChunks; u += kThreads) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (nacc > 0) {
+        float4 w[kAccWays];
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+        for (int m = 0; m < kAccWays; ++m)
+          if (m < nacc) w[m] = __ldcg(acc + u + m * stride4);
+        v = w[0];
 #pragma unroll
-            for (int m = 0; m < kAccWays; ++m)
-              if (m < nacc && i0 + h * kThreads < n4) w[h][m] = __ldcg(acc + i0 + h * kThreads + m * stride4);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int i = i0 + h * kThreads;
-            if (i >= n4) break;
-            float4 v = w[h][0];
-#pragma unroll
-            for (int m = 1; m < kAccWays; ++m) {
-              if (m < nacc) {
-                v.x += w[h][m].x; v.y += w[h][m].y; v.z += w[h][m].z; v.w += w[h][m].w;
-              }
-            }
-            out[i] = make_uint2(pack_bf16x2(p.scale * v.x, p.scale * v.y),
-                                pack_bf16x2(p.scale * v.z, p.scale * v.w));
+        for (int m = 1; m < kAccWays; ++m) {
+          if (m < nacc) {
+            v.x += w[m].x; v.y += w[m].y; v.z += w[m].z; v.w += w[m].w;
           }
         }
+        v.x *= p.scale; v.y *= p.scale; v.z *= p.scale; v.w *= p.scale;
       }
-    } else {
-      // chunk-major tile: chunk units u = chunk * 128 + row, consecutive
-      // threads on consecutive rows (coalesced 16-byte loads); the bf16
-      // result is staged in shared memory (free once the roles are done)
-      // and written row by row
-      const float4* acc = reinterpret_cast<const float4*>(p.dqacc) + ((size_t)bh * p.N + j) * (kTile * kChunks);
-      for (int u = tid; u < kTile * kChunks; u += kThreads) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (nacc > 0) {
-          float4 w[kAccWays];
-#pragma unroll
-          for (int m = 0; m < kAccWays; ++m)
-            if (m < nacc) w[m] = __ldcg(acc + u + m * stride4);
-          v = w[0];
-#pragma unroll
-          for (int m = 1; m < kAccWays; ++m) {
-            if (m < nacc) {
-              v.x += w[m].x; v.y += w[m].y; v.z += w[m].z; v.w += w[m].w;
-            }
-          }
-          v.x *= p.scale; v.y *= p.scale; v.z *= p.scale; v.w *= p.scale;
-        }
-        const int row = u % kTile, ch = u / kTile;
-        *reinterpret_cast<uint2*>(smem + row * kRowBytes + ch * 8) =
-            make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-      }
-      __syncthreads();
-      uint4* out = reinterpret_cast<uint4*>(p.dq + ((size_t)bh * p.S + (size_t)j * kTile) * HD);
-      for (int w = tid; w < rows * (HD / 8); w += kThreads) {
-        const int row = w / (HD / 8), piece = w % (HD / 8);
-        out[w] = *reinterpret_cast<const uint4*>(smem + row * kRowBytes + piece * 16);
-      }
+      const int row = u % kTile, ch = u / kTile;
+      *reinterpret_cast<uint2*>(smem + row * kRowBytes + ch * 8) =
+          make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
+    __syncthreads();
+    uint4* out = reinterpret_cast<uint4*>(p.dq + ((size_t)bh * p.S + (size_t)j * kTile) * HD);
+    for (int w = tid; w < rows * (HD / 8); w += kThreads) {
+      const int row = w / (HD / 8), piece = w % (HD / 8);
+      out[w] = *reinterpret_cast<const uint4*>(smem + row * kRowBytes + piece * 16);
     }
     __syncthreads();  // misc->conv and the staging rows are rewritten for the next tile
   }
@@ -288,8 +251,10 @@ __device__ __forceinline__ void tail_convert(const BwdParams& p, Misc* misc, uin
 
 // kRagged: S is not a multiple of the tile, so the last tile of each head is
 // partial (masked keys, rows never written).  A separate instance, so that the
-// common case carries none of those checks.
-template <int HD, bool kRagged>
+// common case carries none of those checks.  kCM: the dQ accumulation tiles
+// are chunk-major [d/4][128][4] (every schedule at d = 64, the ordered ones at
+// d = 128); otherwise row-major [row][d] (the atomic schedule at d = 128).
+template <int HD, bool kRagged, bool kCM>
 __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = Cfg<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -422,8 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     //     previous dQ partial, which shares them; d = 64: the softmax has
     //     read the previous dP);
     //   warp 2, the "backward" products: dV += P^T dO once the softmax has
-    //     written P, then the dQ partial (d = 128: dQ^T = K^T dS^T; d = 64:
-    //     dQ = dS K) and dK += dS^T Q once it has written dS.
+    //     written P, then the dQ partial (dQ = dS K; dQ^T = K^T dS^T for the
+    //     atomic schedule's row-major accumulator at d = 128) and
+    //     dK += dS^T Q once it has written dS.
     // A commit tracks only the MMAs of the thread that issues it, so the
     // barriers that release a Q/dO stage and the K/V tiles take one commit
     // from each issuer.
@@ -502,15 +468,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
                        k == 0 ? acc0 : 1u);
             }
             mma_commit(&bars->dv_done);
-            // dQ partial (d = 128: dQ^T = K^T dS^T; d = 64: dQ = dS K)
+            // dQ partial (dQ = dS K, or dQ^T = K^T dS^T for a row-major accumulator)
             if (!mbar_wait(&bars->ds_full, s & 1, wc, 17)) { ok = false; break; }
             if (HD == 64 && s > 0 && !mbar_wait(&bars->dq_empty, (s - 1) & 1, wc, 18)) { ok = false; break; }
             tc_fence_after();
+            // dQ = dS K (lanes = Q rows) for a chunk-major accumulator,
+            // dQ^T = K^T dS^T (lanes = d) for a row-major one
+            if (kCM) {
 #pragma unroll
-            for (int k = 0; k < kTile / 16; ++k) {
-              const uint64_t a = ((HD == 128) ? dK_mn : dDS_mn) + koff_mnmajor(k);
-              const uint64_t b = ((HD == 128) ? dDS_mn : dK_mn) + koff_mnmajor(k);
-              mma_ss(tDQ, a, b, C::kIdDQ, k > 0);
+              for (int k = 0; k < kTile / 16; ++k)
+                mma_ss(tDQ, dDS_mn + koff_mnmajor(k), dK_mn + koff_mnmajor(k), C::kIdDQ, k > 0);
+            } else {
+#pragma unroll
+              for (int k = 0; k < kTile / 16; ++k)
+                mma_ss(tDQ, dK_mn + koff_mnmajor(k), dDS_mn + koff_mnmajor(k), C::kIdDQ, k > 0);
             }
             mma_commit(&bars->dq_full);
             // dK += dS^T Q
@@ -787,17 +758,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         const size_t sem_idx = (((size_t)bh * p.N + st.q) * kSubTiles + sub) * p.acc_ways + way;
         const bool store = deterministic && lrank == 0;  // a buffer's first contribution overwrites
         float* acc = p.dqacc + (size_t)way * (size_t)p.acc_stride;
-        // d = 128: row-major, this thread's column of Q rows 64*half ..;
-        // d = 64: chunk-major, this thread's row in its first chunk
+        // chunk-major: this thread's row in its first chunk; row-major
+        // (atomic, d = 128): this thread's column of Q rows 64*half ..
+        constexpr bool cm = kCM;
         const size_t row0 = (size_t)bh * p.S + (size_t)st.q * kTile;
-        float* base = C::kChunkMajor
-                          ? acc + (((size_t)(bh * p.N + st.q) * C::kChunks + (size_t)half * (C::kChunks / 2)) * kTile + r) * 4
-                          : acc + (row0 + (size_t)half * 64) * HD + r;
-        // d = 128: rows past the end of a partial last Q tile belong to the
-        // next head in the row-major accumulator and are never touched (their
-        // partial sums are zero).  d = 64: they lie in the tile's padding.
+        float* base = cm ? acc + (((size_t)(bh * p.N + st.q) * C::kChunks + (size_t)half * (C::kChunks / 2)) * kTile + r) * 4
+                         : acc + (row0 + (size_t)half * 64) * HD + r;
+        // Rows past the end of a partial last Q tile: in a chunk-major tile
+        // they lie in the tile's padding; in the row-major accumulator they
+        // belong to the next head and are never touched (their partial sums
+        // are zero).
         const int row_lim = p.S - st.q * kTile - half * 64;
-        const int nvalid = (!kRagged || C::kChunkMajor) ? 64 : (row_lim < 0 ? 0 : (row_lim > 64 ? 64 : row_lim));
+        const int nvalid = !kRagged ? 64 : (row_lim < 0 ? 0 : (row_lim > 64 ? 64 : row_lim));
         if (!warp_wait(&bars->dq_full, s & 1, wc, 41)) { ok = false; break; }
         tc_fence_after();
         uint32_t v[kVals];
@@ -813,41 +785,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           if (lane == 0) g = sem_wait(p.sem + sem_idx, (uint32_t)lrank, wc, (uint32_t)sem_idx) ? 1 : 0;
           g = __shfl_sync(0xffffffffu, g, 0);
           if (!g) { ok = false; break; }
-          if (p.plain_add && !store) fence_acq_rel_gpu();
+          // Lane 0's acquire observed the previous rank's release; the warp
+          // barrier orders that acquire before every lane's adds (or, with
+          // DAB_BWD_PLAIN_ADD, loads), so each lane sees the previous rank's
+          // sums and adds after them.
+          __syncwarp();
         }
         // one straight-line loop per kind of add (no per-element branch)
-        if (HD == 128) {
-          if (store) {
+        if (HD == 128 && !cm) {
+          // row-major (atomic only): a warp's 32 adds of a row are 128
+          // contiguous bytes
 #pragma unroll
-            for (int q = 0; q < 64; ++q)
-              if (q < nvalid) base[(size_t)q * HD] = __uint_as_float(v[q]);
-          } else if (deterministic && p.plain_add) {
-            // load + add + store, the same IEEE adds in the same order as
-            // the red (only this contributor touches the sub-tile now)
-#pragma unroll
-            for (int c = 0; c < 64; c += 16) {
-              float a[16];
-#pragma unroll
-              for (int k = 0; k < 16; ++k)
-                a[k] = (c + k < nvalid) ? ld_cg_f32(base + (size_t)(c + k) * HD) : 0.f;
-#pragma unroll
-              for (int k = 0; k < 16; ++k)
-                if (c + k < nvalid) base[(size_t)(c + k) * HD] = a[k] + __uint_as_float(v[c + k]);
-            }
-          } else if (deterministic) {
-#pragma unroll
-            for (int q = 0; q < 64; ++q) {
-              if (q < nvalid) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
-              // spread the adds out so that they do not fill the SM's
-              // memory-instruction queue in one burst (the softmax warps'
-              // shared-memory loads wait behind them)
-              if ((q & 7) == 7) __nanosleep(20);
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 64; ++q)
-              if (q < nvalid) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
-          }
+          for (int q = 0; q < 64; ++q)
+            if (q < nvalid) red_add_f32(base + (size_t)q * HD, __uint_as_float(v[q]));
         } else {
           if (store) {
 #pragma unroll
@@ -856,14 +806,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
                   make_float4(__uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
                               __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
           } else if (deterministic && p.plain_add) {
-            // load + add + store: the same IEEE adds in the same order
+            // load + add + store: the same IEEE adds in the same order as the
+            // red (only this contributor touches the sub-tile now); four
+            // loads in flight before their stores
 #pragma unroll
-            for (int m = 0; m < kVals / 4; ++m) {
-              float* dst = base + (size_t)m * (kTile * 4);
-              const float4 b = ld_cg_v4_f32(dst);
-              *reinterpret_cast<float4*>(dst) =
-                  make_float4(b.x + __uint_as_float(v[4 * m]), b.y + __uint_as_float(v[4 * m + 1]),
-                              b.z + __uint_as_float(v[4 * m + 2]), b.w + __uint_as_float(v[4 * m + 3]));
+            for (int m0 = 0; m0 < kVals / 4; m0 += 4) {
+              float4 b[4];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) b[m] = ld_cg_v4_f32(base + (size_t)(m0 + m) * (kTile * 4));
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const int e = 4 * (m0 + m);
+                *reinterpret_cast<float4*>(base + (size_t)(m0 + m) * (kTile * 4)) =
+                    make_float4(b[m].x + __uint_as_float(v[e]), b[m].y + __uint_as_float(v[e + 1]),
+                                b[m].z + __uint_as_float(v[e + 2]), b[m].w + __uint_as_float(v[e + 3]));
+              }
             }
           } else {
 #pragma unroll
@@ -892,6 +849,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  // The tail convert reads chunk-major tiles: only the ordered schedules set
+  // fuse_convert, and they always run a kCM instance.  (It is compiled into
+  // the row-major instance too: without it that instance ran 3 % slower.)
   if (p.fuse_convert) tail_convert<HD, kRagged>(p, misc, smem, wc);
 }
 
@@ -903,14 +863,18 @@ int bwd_smem_bytes() {
 }
 
 template <int HD>
-const void* bwd_kernel_ptr(bool ragged) {
-  return ragged ? reinterpret_cast<const void*>(&bwd_kernel<HD, true>)
-                : reinterpret_cast<const void*>(&bwd_kernel<HD, false>);
+const void* bwd_kernel_ptr(bool ragged, bool chunk_major) {
+  static_assert(HD == 64 || HD == 128, "head dim");
+  if (HD == 64 || chunk_major)
+    return ragged ? reinterpret_cast<const void*>(&bwd_kernel<HD, true, true>)
+                  : reinterpret_cast<const void*>(&bwd_kernel<HD, false, true>);
+  return ragged ? reinterpret_cast<const void*>(&bwd_kernel<HD, true, (HD == 64)>)
+                : reinterpret_cast<const void*>(&bwd_kernel<HD, false, (HD == 64)>);
 }
 
 template int bwd_smem_bytes<64>();
 template int bwd_smem_bytes<128>();
-template const void* bwd_kernel_ptr<64>(bool);
-template const void* bwd_kernel_ptr<128>(bool);
+template const void* bwd_kernel_ptr<64>(bool, bool);
+template const void* bwd_kernel_ptr<128>(bool, bool);
 
 }  // namespace dab

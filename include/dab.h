@@ -135,9 +135,10 @@ size_t dab_bwd_workspace_size(int B, int H, int S, int d,
  *      contributor adds its partial only once every contributor of lower
  *      rank in the same buffer has published, so each element receives its
  *      additions in one fixed order.  By default that addition is a float
- *      reduction in the L2 (red.add.f32), issued by one contributor at a
- *      time; DAB_BWD_PLAIN_ADD replaces it with a load, an add in registers
- *      and a store, which gives the same bits and uses no float atomic;
+ *      reduction in the L2 (red.add.v4.f32: four f32 adds per 16-byte
+ *      vector), issued by one contributor at a time; DAB_BWD_PLAIN_ADD
+ *      replaces it with a load, an add in registers and a store, which gives
+ *      the same bits and uses no float atomic;
  *   3. for ATOMIC only: the convert kernel, the same dQ formula as a separate
  *      pass (see DAB_BWD_SEPARATE_CONVERT).
  * The call returns once the kernels are queued.                              */
@@ -262,8 +263,9 @@ typedef struct {
     size_t sem;      /* uint32 [B*H][N][8][ways] semaphores                     */
     size_t D;        /* float  [B*H*Spad], heads padded to whole 128-row tiles  */
     size_t lse2;     /* float  [B*H*Spad] -LSE * log2(e), heads padded to tiles */
-    size_t dqacc;    /* float  [ways][B*H*Spad*d]: d = 128 row-major [row][d];
-                        d = 64 per 128-row tile [d/4][128][4]                  */
+    size_t dqacc;    /* float  [ways][B*H*Spad*d]: per 128-row tile
+                        [d/4][128][4] (chunk-major), except the atomic
+                        schedule at d = 128: row-major [row][d]                */
     size_t total;
 } dab_ws_layout_t;
 
