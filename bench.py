@@ -40,11 +40,11 @@ DET_SCHEDS = ("serial", "descending_q", "shift")
 # with the number of heads, so the B=2 launch moves twice as much.  Reported
 # only while the source is unchanged.
 TRAFFIC_CAPTURES = {
-    "cbca788546cba291a7f9ead4cfa106c034cf818b": {
-        "causal/serial": 468.7 + 407.8, "causal/descending_q": 393.1 + 353.1,
-        "causal/shift": 464.6 + 472.7, "causal/atomic": 202.8 + 88.4,
-        "full/serial": 398.8 + 361.7, "full/descending_q": 399.0 + 366.0,
-        "full/shift": 443.3 + 466.8, "full/atomic": 202.6 + 87.7,
+    "ea20e201b8cebb1c76e0983b4b8cddd964e30e4f": {
+        "causal/serial": 466.8 + 397.8, "causal/descending_q": 393.4 + 351.8,
+        "causal/shift": 455.0 + 462.5, "causal/atomic": 202.9 + 89.0,
+        "full/serial": 398.8 + 360.9, "full/descending_q": 399.8 + 363.6,
+        "full/shift": 433.9 + 443.5, "full/atomic": 202.6 + 88.6,
     },
 }
 MASKS = ("causal", "full")

@@ -222,12 +222,10 @@ def test_sched_select_picks_a_runnable_deterministic_schedule():
     assert lib.dab_sched_select(0, 1, 1, 256, 0) == -1
 
 
-SHIFT_PENALTY = 1.025  # the selector's factor on SHIFT's predicted makespan
 
 
 def test_sched_select_follows_the_model():
-    """The pick is the model's argmin, SHIFT's makespan raised by the
-    documented factor (ties to descending_q, then serial)."""
+    """The pick is the model's argmin (ties to descending_q, then serial)."""
     for mask, B, H, S in (("causal", 2, 4, 2048), ("full", 1, 8, 4096), ("full", 2, 16, 8192),
                           ("full", 4, 16, 2048)):
         N = S // 128
@@ -235,7 +233,7 @@ def test_sched_select_follows_the_model():
         for s in ("descending_q", "serial", "shift"):
             rc, m, _ = dab.dag_simulate(s, mask, N, B * H, 152, 1.0, 1.0, 1, ways=4)
             if rc == 0 and dab.sched_gang_size(s, mask, N) <= 152:
-                mk[s] = m * (SHIFT_PENALTY if s == "shift" else 1.0)
+                mk[s] = m
         best = min(mk.values())
         expect = next(s for s in ("descending_q", "serial", "shift") if s in mk and mk[s] <= best * (1 + 1e-9))
         assert dab.sched_select(mask, B, H, S, 152) == expect
@@ -243,10 +241,11 @@ def test_sched_select_follows_the_model():
 
 def test_sched_select_matches_the_measured_gb300_winners():
     """At the benchmark workload (B=2, H=16, S=8192, 152 CTAs) the GB300
-    measurements have SHIFT fastest under the causal mask and DESCENDING_Q
-    under the full mask; at B=4, H=16, S=2048 SHIFT is fastest for both."""
+    measurements have SHIFT fastest under both masks (full: 3.08 ms against
+    3.16 for DESCENDING_Q); at B=4, H=16, S=2048 the full mask is a tie
+    within 0.3 % and SHIFT is picked."""
     assert dab.sched_select("causal", 2, 16, 8192, 152) == "shift"
-    assert dab.sched_select("full", 2, 16, 8192, 152) == "descending_q"
+    assert dab.sched_select("full", 2, 16, 8192, 152) == "shift"
     assert dab.sched_select("full", 4, 16, 2048, 152) == "shift"
     assert dab.sched_select("causal", 4, 16, 2048, 152) == "shift"
 
