@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       mbar_init(&bars->q_empty[s], 2 + 8);
       mbar_init(&bars->unit_full[s], 1);
       mbar_init(&bars->unit_empty[s], 2 + 8 + 8 + 1);
-      mbar_init(&bars->pub_full[s], 8 * 32);
+      mbar_init(&bars->pub_full[s], 8);
       mbar_init(&bars->pub_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
@@ -512,10 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   } else if (warp == 3) {
     // ------------------------------------------------------ dQ publisher
     // Ordered schedules only (ATOMIC has no semaphores: this warp just
-    // follows the units).  Every reducer thread arrives (release, CTA scope)
-    // on pub_full after its adds of a step; this warp acquires that phase
-    // and then, per eighth (lane k: eighth k), fences at gpu scope and stores
-    // rank + 1.  A release is cumulative: the adds ordered before the arrive
+    // follows the units).  Every reducer warp arrives (release, CTA scope)
+    // on pub_full after a warp barrier behind its adds of a step; this warp
+    // acquires that phase and then, per eighth (lane k: eighth k), fences at
+    // gpu scope and stores rank + 1.  A release is cumulative: the adds ordered before the arrive
     // that the acquire observed are ordered before the semaphore store for
     // whoever acquires it.  So the reducer warps do not wait for their adds
     // to be performed before draining and adding the next partial.
@@ -830,13 +830,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           }
         }
         if (deterministic) {
-          // Hand the release of rank + 1 to the publisher: every thread
-          // arrives (release, CTA scope) after its adds.  The slot of this
-          // parity is free once the publisher has released step s - 2.
+          // Hand the release of rank + 1 to the publisher.  The warp barrier
+          // orders every lane's adds before lane 0's arrive (release, CTA
+          // scope), so one arrive per warp carries the whole warp's adds
+          // (256 arrives per step cost 1 % more).  The slot of this parity
+          // is free once the publisher has released step s - 2.
           if (s >= 2 && !warp_wait(&bars->pub_empty[s & 1], ((s >> 1) - 1) & 1, wc, 44)) { ok = false; break; }
           if (lane == 0) slots[(s & 1) * kSubTiles + sub] = make_uint2((uint32_t)sem_idx, (uint32_t)lrank + 1u);
           __syncwarp();
-          mbar_arrive(&bars->pub_full[s & 1]);
+          if (lane == 0) mbar_arrive(&bars->pub_full[s & 1]);
         }
         ++s;
       }
