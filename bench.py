@@ -40,11 +40,11 @@ DET_SCHEDS = ("serial", "descending_q", "shift")
 # with the number of heads, so the B=2 launch moves twice as much.  Reported
 # only while the source is unchanged.
 TRAFFIC_CAPTURES = {
-    "ea20e201b8cebb1c76e0983b4b8cddd964e30e4f": {
-        "causal/serial": 466.8 + 397.8, "causal/descending_q": 393.4 + 351.8,
-        "causal/shift": 455.0 + 462.5, "causal/atomic": 202.9 + 89.0,
-        "full/serial": 398.8 + 360.9, "full/descending_q": 399.8 + 363.6,
-        "full/shift": 433.9 + 443.5, "full/atomic": 202.6 + 88.6,
+    "2015f156a7f1bac992497fc2361746d1bda80c34": {
+        "causal/serial": 447.5 + 390.9, "causal/descending_q": 393.1 + 351.7,
+        "causal/shift": 450.9 + 451.5, "causal/atomic": 202.7 + 88.8,
+        "full/serial": 400.3 + 365.0, "full/descending_q": 400.8 + 366.4,
+        "full/shift": 436.6 + 439.7, "full/atomic": 202.6 + 88.4,
     },
 }
 MASKS = ("causal", "full")

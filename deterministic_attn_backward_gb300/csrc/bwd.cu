@@ -514,11 +514,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     // Ordered schedules only (ATOMIC has no semaphores: this warp just
     // follows the units).  Every reducer warp arrives (release, CTA scope)
     // on pub_full after a warp barrier behind its adds of a step; this warp
-    // acquires that phase and then, per eighth (lane k: eighth k), fences at
-    // gpu scope and stores rank + 1.  A release is cumulative: the adds ordered before the arrive
-    // that the acquire observed are ordered before the semaphore store for
-    // whoever acquires it.  So the reducer warps do not wait for their adds
-    // to be performed before draining and adding the next partial.
+    // acquires that phase and then, per eighth (lane k: eighth k), stores
+    // rank + 1 with a gpu-scope release.  Release is cumulative: the adds
+    // ordered before the arrive that the acquire observed are ordered before
+    // the semaphore store for whoever acquires it.  So the reducer warps do
+    // not wait for their adds to be performed before draining and adding the
+    // next partial.  (Without the release the dQ bits changed between runs.)
     const uint2* slots = reinterpret_cast<const uint2*>(smem + C::kOffPub);
     int s = 0, uidx = 0;
     bool ok = true;
@@ -536,7 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           if (!warp_wait(&bars->pub_full[s & 1], (s >> 1) & 1, wc, 53)) { ok = false; break; }
           if (lane < kSubTiles) {
             const uint2 e = slots[(s & 1) * kSubTiles + lane];
-            fence_acq_rel_gpu();
+            // a release store: the reducers' adds precede it in causality
+            // order (their CTA-scope release, this warp's acquire), so it
+            // publishes them at gpu scope without a separate fence
             st_release_gpu(p.sem + e.x, e.y);
           }
           __syncwarp();
