@@ -36,11 +36,12 @@ DET_SCHEDS = ("serial", "descending_q", "shift")
 
 # DRAM bytes (read + write, MB) of one main-kernel launch at B=1, H=16,
 # S=8192, d=128 per (mask, schedule), from ncu captures of that launch,
-# keyed by the SHA-1 of the kernel source they were taken on.  Traffic scales
-# with the number of heads, so the B=2 launch moves twice as much.  Reported
-# only while the source is unchanged.
+# keyed by the SHA-1 of the kernel source they were taken on (or of a source
+# that differs from it in comments only).  Traffic scales with the number of
+# heads, so the B=2 launch moves twice as much.  Reported only while the
+# source is unchanged.
 TRAFFIC_CAPTURES = {
-    "2015f156a7f1bac992497fc2361746d1bda80c34": {
+    "a9dfccfe777b0e9a31658b1875b33c304bdb74a8": {
         "causal/serial": 447.5 + 390.9, "causal/descending_q": 393.1 + 351.7,
         "causal/shift": 450.9 + 451.5, "causal/atomic": 202.7 + 88.8,
         "full/serial": 400.3 + 365.0, "full/descending_q": 400.8 + 366.4,

@@ -722,12 +722,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     // tensor-memory quadrant of the dQ partial into registers at once (so
     // the tensor memory is free for the next partial), then adds that
     // eighth of the tile into the f32 accumulator:
-    //   d = 128 (dQ^T, lanes = d): d index 32*quad + lane, Q rows
-    //     64*half .. + 63; each add is one float, a warp's 32 adds of a row
-    //     are 128 contiguous bytes of the row-major accumulator;
-    //   d = 64 (dQ, lanes = Q rows): Q row 32*quad + lane, d columns
-    //     32*half .. + 31; each add is 16 bytes into the chunk-major tile
-    //     [d/4][128][4], a warp's 32 rows of a chunk are 512 contiguous bytes.
+    //   chunk-major (dQ, lanes = Q rows): Q row 32*quad + lane, d columns
+    //     (d/2)*half .. + d/2 - 1; each add is 16 bytes into the tile
+    //     [d/4][128][4], a warp's 32 rows of a chunk are 512 contiguous bytes;
+    //   row-major (atomic at d = 128; dQ^T, lanes = d): d index
+    //     32*quad + lane, Q rows 64*half .. + 63; each add is one float, a
+    //     warp's 32 adds of a row are 128 contiguous bytes.
     // For the ordered schedules every eighth of every accumulation buffer has
     // its own semaphore, so consecutive contributors to one dQ tile overlap
     // on different eighths and buffers while each element of a buffer still
@@ -736,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     const int quad = warp & 3;                          // tensor-memory lane quadrant
     const int half = (warp - kReducerWarp0) >> 2;
     const int sub = half * 4 + quad;                    // sub-tile / semaphore index
-    const int r = quad * 32 + lane;                     // d index (d = 128) or Q row (d = 64)
+    const int r = quad * 32 + lane;                     // Q row (chunk-major) or d index (row-major)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     constexpr int kVals = (HD == 128) ? 64 : 32;        // values per thread per step
     uint2* slots = reinterpret_cast<uint2*>(smem + C::kOffPub);
