@@ -41,11 +41,11 @@ DET_SCHEDS = ("serial", "descending_q", "shift")
 # heads, so the B=2 launch moves twice as much.  Reported only while the
 # source is unchanged.
 TRAFFIC_CAPTURES = {
-    "a9dfccfe777b0e9a31658b1875b33c304bdb74a8": {
-        "causal/serial": 447.5 + 390.9, "causal/descending_q": 393.1 + 351.7,
-        "causal/shift": 450.9 + 451.5, "causal/atomic": 202.7 + 88.8,
-        "full/serial": 400.3 + 365.0, "full/descending_q": 400.8 + 366.4,
-        "full/shift": 436.6 + 439.7, "full/atomic": 202.6 + 88.4,
+    "a1187a10e664449de754d08b0cce1bf6b0e2a036": {
+        "causal/serial": 461.5 + 401.4, "causal/descending_q": 393.0 + 350.6,
+        "causal/shift": 446.8 + 448.6, "causal/atomic": 202.8 + 88.3,
+        "full/serial": 399.1 + 363.4, "full/descending_q": 399.2 + 363.6,
+        "full/shift": 432.6 + 441.5, "full/atomic": 202.6 + 87.8,
     },
 }
 MASKS = ("causal", "full")
