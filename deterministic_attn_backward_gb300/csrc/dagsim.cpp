@@ -233,8 +233,8 @@ extern "C" double dab_dag_critical_path(int sched, int mask, int N, double wc, d
 // trailing the compute, four interleaved accumulation buffers), picks the
 // deterministic schedule with the smallest predicted makespan.  On the GB300
 // sweep (29 shapes, d 64 and 128, S 1024 to 32768, both masks) its pick is
-// the measured fastest deterministic schedule in 24; the summed loss against
-// the measured best is 3.5 %, the largest 2.1 % (B4 H16 S8192 d128, full
+// the measured fastest deterministic schedule in 27; the summed loss against
+// the measured best is 1.4 %, the largest 1.1 % (B4 H16 S8192 d128, full
 // mask, where SHIFT ran faster than predicted).  An extra penalty on SHIFT's
 // prediction (its statically placed rings run in lock step) helped an
 // earlier kernel whose reduction was slower; with this kernel any penalty
